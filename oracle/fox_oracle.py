@@ -1,0 +1,234 @@
+"""CPU fp64 oracle for forget-gated causal softmax attention (FoX).
+
+TEST INFRASTRUCTURE ONLY. This module is the plain, slow, obviously-correct
+statement of what the CUDA path computes. Only the test suite, the smoke check
+of the package entry file and the benchmark's CPU-baseline / reference arm may
+import it; the library and its Python binding never do.
+
+Sources (web pages, cited by title and section):
+  [FoX-module]  "Forgetting Transformer (FoX) Attention" module source
+                (frankenstein-transformer docs, fox_attn), class
+                ForgettingAttention: module docstring formula and forward().
+  [foxwindow]   foxwindow README, sections "The window is a first-passage time"
+                and "ALiBi is the zero-variance limit".
+  [fast-tf]     fast-transformers "Creating a custom attention layer",
+                section "New Attention" (inputs already projected and split
+                into heads; einsum layout "nlhe,nshe->nhls", i.e. [B, N, H, d]).
+
+Notation: tokens t = 0..N-1 per (batch b, head h); a_t = log f_t with
+f_t = sigmoid(z_t); c_t = sum_{l<=t} a_l; scale defaults to d^-1/2.
+
+Readings taken where the pages are silent or disagree (each also a flag or a
+fixed choice here):
+  * Lower summation limit. The module docstring writes D_ij = sum_{l=j}^{i}
+    log f_l; the module's code (cumsum then outer difference) and the foxwindow
+    score form give sum_{l=j+1}^{i}. Both are implemented: bias_from_j=False
+    (default) is j+1, so D_ii = 0; bias_from_j=True is j.
+  * The module adds 1e-6 inside the log. The formula in both pages has no such
+    term; the oracle uses the exact log-sigmoid.
+  * The scale multiplies q.k only, never D (module forward()).
+  * Always causal (the module's "decoder" mode); no dropout.
+  * LSE (not on the pages) is the natural-log normaliser of the biased,
+    scaled scores, per row, layout [B, N, H].
+  * z = +inf means f = 1 exactly (log f = 0).
+  * The backward pass is not on the pages; it is the chain rule through the
+    same forward formula.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "log_forget_gate",
+    "cumulative_log_gate",
+    "forget_bias",
+    "attention_head",
+    "attention_rows",
+    "forward",
+    "backward_head",
+    "backward",
+    "gate_grad_bruteforce",
+    "default_scale",
+]
+
+
+def default_scale(d: int) -> float:
+    """d^-1/2 [FoX-module, __init__: scale = head_dim ** -0.5]."""
+    return float(d) ** -0.5
+
+
+def log_forget_gate(z) -> np.ndarray:
+    """a = log sigmoid(z) in fp64 [FoX-module, forward(): sigmoid of the gate
+    projection, then its log].
+
+    Evaluated as min(z, 0) - log1p(exp(-|z|)), which equals log(1/(1+e^-z))
+    for every real z without overflow; z = +inf gives exactly 0.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.minimum(z, 0.0) - np.log1p(np.exp(-np.abs(z)))
+
+
+def cumulative_log_gate(a: np.ndarray) -> np.ndarray:
+    """c_t = sum_{l<=t} a_l along the last axis [FoX-module, forward(): cumsum of log f]."""
+    return np.cumsum(np.asarray(a, dtype=np.float64), axis=-1)
+
+
+def forget_bias(a: np.ndarray, bias_from_j: bool = False) -> np.ndarray:
+    """D [N, N] for one head, from its log gates a [N].
+
+    j+1 convention: D_ij = sum_{l=j+1}^{i} a_l = c_i - c_j
+        [FoX-module, forward(): outer difference of the cumsum;
+         foxwindow, "The window is a first-passage time": score form].
+    j convention:   D_ij = sum_{l=j}^{i} a_l = c_i - c_{j-1}, c_{-1} = 0
+        [FoX-module, module docstring formula].
+    Entries above the diagonal are returned as computed; the causal mask is
+    applied by the caller.
+    """
+    c = cumulative_log_gate(a)
+    col = c - a if bias_from_j else c
+    return c[:, None] - col[None, :]
+
+
+def attention_head(q, k, v, z, scale=None, bias_from_j=False, return_p=False):
+    """Forward of one (b, h): q, k, v [N, d], z [N] -> O [N, d], LSE [N].
+
+    S_ij = scale * q_i . k_j + D_ij for j <= i, -inf for j > i
+        [FoX-module, forward(): logits (q @ k^T) * scale + bias, causal
+         triu(diagonal=1) mask set to -inf in decoder mode];
+    LSE_i = M_i + ln sum_j exp(S_ij - M_i), M_i = max_j S_ij;
+    P_ij = exp(S_ij - LSE_i) [FoX-module, forward(): softmax over keys];
+    O_i = sum_j P_ij v_j [FoX-module, forward(): attn @ v].
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    if N == 0:
+        empty = (np.zeros((0, v.shape[1])), np.zeros(0))
+        return empty + (np.zeros((0, 0)),) if return_p else empty
+    D = forget_bias(log_forget_gate(z), bias_from_j)
+    S = scale * (q @ k.T) + D
+    S[np.triu(np.ones((N, N), dtype=bool), k=1)] = -np.inf
+    M = S.max(axis=1)
+    lse = M + np.log(np.exp(S - M[:, None]).sum(axis=1))
+    P = np.exp(S - lse[:, None])
+    O = P @ v
+    return (O, lse, P) if return_p else (O, lse)
+
+
+def attention_rows(q, k, v, z, rows, scale=None, bias_from_j=False):
+    """The forward of one (b, h) restricted to the query rows `rows`.
+
+    Row i of O and LSE depends only on row i of S, so this is the same
+    definition as attention_head evaluated for the listed rows only (used for
+    sequences too long to hold S whole).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    a = log_forget_gate(z)
+    c = cumulative_log_gate(a)
+    col = c - a if bias_from_j else c
+    rows = np.asarray(rows, dtype=np.int64)
+    O = np.empty((rows.size, v.shape[1]))
+    lse = np.empty(rows.size)
+    for n, i in enumerate(rows):
+        s = scale * (k[: i + 1] @ q[i]) + (c[i] - col[: i + 1])
+        m = s.max()
+        lse[n] = m + np.log(np.exp(s - m).sum())
+        O[n] = np.exp(s - lse[n]) @ v[: i + 1]
+    return O, lse
+
+
+def forward(q, k, v, z, scale=None, bias_from_j=False):
+    """Batched forward. q, k, v [B, N, H, d]; z [B, N, H] -> O [B, N, H, d], LSE [B, N, H].
+
+    Layout per [fast-tf, "New Attention"]: inputs already projected and split
+    into heads, [batch, length, heads, dim]; every (b, h) is independent.
+    """
+    q = np.asarray(q, np.float64)
+    B, N, H, d = q.shape
+    O = np.empty((B, N, H, v.shape[-1]))
+    lse = np.empty((B, N, H))
+    for b in range(B):
+        for h in range(H):
+            O[b, :, h], lse[b, :, h] = attention_head(
+                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], scale, bias_from_j
+            )
+    return O, lse
+
+
+def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=False):
+    """Gradients of one (b, h) by the chain rule through attention_head.
+
+    dP_ij = dO_i . v_j;  Delta_i = dO_i . O_i;  dS_ij = P_ij (dP_ij - Delta_i)
+    dV_j = sum_i P_ij dO_i;  dQ_i = scale sum_j dS_ij k_j;  dK_j = scale sum_i dS_ij q_i
+    Gate: R_i = sum_j dS_ij (row sums), C_j = sum_i dS_ij (column sums).
+      j+1: d a_t = sum_{s>=t} (R_s - C_s)
+      j  : d a_t = sum_{s>=t} (R_s - C_s) + C_t
+    (a reverse prefix sum; gate_grad_bruteforce states the same quantity as
+    the double sum over the entries of D that contain a_t), and
+    dz_t = d a_t * sigmoid(-z_t), since d/dz log sigmoid(z) = sigmoid(-z).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    dO = np.asarray(dO, np.float64)
+    z = np.asarray(z, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    O, lse, P = attention_head(q, k, v, z, scale, bias_from_j, return_p=True)
+    dP = dO @ v.T
+    delta = (dO * O).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    dV = P.T @ dO
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q)
+    R = dS.sum(axis=1)
+    C = dS.sum(axis=0)
+    suffix = np.cumsum((R - C)[::-1])[::-1]
+    da = suffix + C if bias_from_j else suffix
+    with np.errstate(over="ignore"):
+        sig_neg = 1.0 / (1.0 + np.exp(z))  # sigmoid(-z); exactly 0 at z = +inf
+    dz = da * sig_neg
+    if return_sums:
+        return dQ, dK, dV, dz, {"R": R, "C": C, "dS": dS, "da": da, "O": O, "lse": lse, "P": P}
+    return dQ, dK, dV, dz
+
+
+def gate_grad_bruteforce(dS: np.ndarray, bias_from_j: bool = False) -> np.ndarray:
+    """d a_t as the plain double sum over the bias entries that contain a_t.
+
+    j+1: a_t is in D_ij iff j < t <= i, so d a_t = sum_{i>=t} sum_{j<t} dS_ij.
+    j  : a_t is in D_ij iff j <= t <= i, so d a_t = sum_{i>=t} sum_{j<=t} dS_ij.
+    O(N^3); for small N only.
+    """
+    N = dS.shape[0]
+    da = np.zeros(N)
+    for t in range(N):
+        jmax = t + 1 if bias_from_j else t
+        da[t] = dS[t:, :jmax].sum()
+    return da
+
+
+def backward(q, k, v, z, dO, scale=None, bias_from_j=False):
+    """Batched backward over [B, N, H, d]: returns dQ, dK, dV [B, N, H, d], dz [B, N, H]."""
+    q = np.asarray(q, np.float64)
+    B, N, H, d = q.shape
+    dQ = np.empty((B, N, H, d))
+    dK = np.empty((B, N, H, d))
+    dV = np.empty((B, N, H, v.shape[-1]))
+    dz = np.empty((B, N, H))
+    for b in range(B):
+        for h in range(H):
+            dQ[b, :, h], dK[b, :, h], dV[b, :, h], dz[b, :, h] = backward_head(
+                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], dO[b, :, h], scale, bias_from_j
+            )
+    return dQ, dK, dV, dz

@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the forget-gated causal attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+gate scan + fused forward (O, LSE), then gate scan + backward rows + fused
+backward + dQ conversion + reverse gate scan (dQ, dK, dV, dz). Throughput is
+nominal causal FLOPs (2 B H N^2 d forward, 5 B H N^2 d backward) per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fox|reference]
+
+Under torchrun each rank runs its own batch of independent (b, h) heads
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+--impl reference times the CPU fp64 oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "FoX causal attention fwd/bwd TFLOP/s (bf16) and % of GB300 tensor-core peak"
+WORKLOAD = wl.Workload(
+    "long_bf16_B1H32N16384d128", 1, 16384, 32, 128, "bf16", 2, gate="head_linspace", lo=0.0, hi=8.0, sigma=0.5,
+    backward=True,
+)
+# CPU sample of the same workload: heads (0, 0..3), each restricted to its first 4096 tokens
+# (a causal prefix is a complete problem of its own), forward + backward.
+CPU_SAMPLE_HEADS = 4
+CPU_SAMPLE_TOKENS = 4096
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; an ncu traffic figure is only reported for the build it was taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "forget_gated_softmax_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes for `kernel` from profiles/ncu_traffic.md, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    pat = re.compile(r"^\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]+)\s*\|")
+    with open(path) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
+                return float(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fox_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def oracle_sample(arrays, heads: int, tokens: int):
+    """Oracle forward + backward on heads (0, 0..heads-1) restricted to their first `tokens` tokens."""
+    from oracle import fox_oracle as ora
+
+    x = {n: (a[0, :tokens, :heads].astype(np.float64) if n == "z" else wl.as_f64(a[0, :tokens, :heads], "bf16"))
+         for n, a in arrays.items()}
+    t0 = time.perf_counter()
+    for h in range(heads):
+        ora.backward_head(x["q"][:, h], x["k"][:, h], x["v"][:, h], x["z"][:, h], x["dO"][:, h])
+    dt = time.perf_counter() - t0
+    flops = heads * 7.0 * tokens * tokens * WORKLOAD.d  # nominal fwd (2) + bwd (5) per head
+    return flops / dt / 1e12, dt
+
+
+def blas_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def sample_desc():
+    return (f"oracle forward+backward of heads (b=0, h=0..{CPU_SAMPLE_HEADS - 1}) of {WORKLOAD.name}, each cut to "
+            f"its first {CPU_SAMPLE_TOKENS} tokens (a causal prefix), fp64 numpy; TFLOP/s on nominal 7*N^2*d per head")
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    arrays = draw_inputs(WORKLOAD, rank, cut=CPU_SAMPLE_TOKENS)
+    for _ in range(args.warmup):
+        oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, dt = oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+        vals.append(v)
+        times.append(dt)
+    total_flops = args.steps * CPU_SAMPLE_HEADS * 7.0 * CPU_SAMPLE_TOKENS**2 * WORKLOAD.d
+    value = total_flops / sum(times) / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample_desc()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(n_gpus: int):
+    w = WORKLOAD
+    return {
+        "workload": f"{w.name}: forward+backward, causal, j+1 convention, q,k,v,dO ~ N(0,1) bf16, "
+                    f"z = b_h + 0.5 N(0,1), b_h = linspace(0, 8, 32)",
+        "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+        "flops_per_step": w.fwd_flops() + w.bwd_flops(),
+        "l2": "inputs larger than L2: q, k, v, dO are 134 MB each, 537 MB read per step",
+        "parallelism": f"{n_gpus} rank(s), each an independent batch of heads (no collective)",
+    }
+
+
+def draw_inputs(w: wl.Workload, rank: int, cut: int = 0):
+    """Seeded inputs; rank r draws the workload with seed + 1000 r (an independent batch of heads).
+    With `cut`, only the first `cut` tokens of every tensor are kept."""
+    import dataclasses
+
+    if rank:
+        w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
+    arrays = wl.draw(w, with_dO=True)
+    if cut:
+        arrays = {n: np.ascontiguousarray(a[:, :cut]) for n, a in arrays.items()}
+    return arrays
+
+
+def run_fox(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import forget_gated_softmax_gb300 as fox
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    w = WORKLOAD
+    t0 = time.time()
+    arrays = draw_inputs(w, rank)
+    log(f"[rank {rank}] inputs drawn in {time.time() - t0:.1f}s")
+
+    def dev(name):
+        a = arrays[name]
+        if name == "z":
+            return torch.from_numpy(a).cuda()
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v, z, dO = (dev(n) for n in ("q", "k", "v", "z", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.N, w.H), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dz = torch.empty_like(lse)
+    pf = fox.make_params(w.B, w.N, w.H, w.d, 0, 0.0, False)
+    ws_f = fox.workspace(fox.fox_fwd_workspace_bytes(pf), "cuda")
+    ws_b = fox.workspace(fox.fox_bwd_workspace_bytes(pf), "cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_f, stream=stream)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream)
+
+    for i in range(args.warmup):
+        step()
+        if i == 0:
+            assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
+    torch.cuda.synchronize()
+
+    # ---------------- device-resident timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        time.sleep(0.3)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        fox.trace_begin()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            stops[i].record(stream)
+        torch.cuda.synchronize()
+        records = fox.trace_end()
+        if dist:
+            dist.barrier()
+    clocks = sampler.summary()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    elapsed_ms = starts[0].elapsed_time(stops[-1])
+    assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
+    if dist:
+        t = torch.tensor([elapsed_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    flops_step = w.fwd_flops() + w.bwd_flops()
+    value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # per-kernel breakdown from the trace (same timed region, events on the launching stream)
+    per = {}
+    for name, ms in records:
+        per.setdefault(name, []).append(ms)
+    peaks, peak_src = measured_peaks()
+    algo = {  # algorithmic work per launch
+        "attn_fwd": ("tensor", w.fwd_flops()),
+        "attn_bwd": ("tensor", w.bwd_flops()),
+        "gate_tile_scan": ("hbm", w.tokens * (4 + 4 + 4 + 4)),   # z in; rowloc, colrec, tile totals out
+        "gate_base_scan": ("hbm", w.B * w.H * ((w.N + 127) // 128) * (4 + 16)),
+        "bwd_rows": ("hbm", w.tokens * (2 * w.d * 2 + 4 + 4 + 4 + 4 + 4 * w.d)),  # O, dO, lse, rowloc in; delta, rho, dQ-acc zero out
+        "bwd_dq": ("hbm", w.tokens * w.d * (4 + 2)),
+        "bwd_gate": ("hbm", w.tokens * (4 + 4 + 4)),
+    }
+    kernels = {}
+    for name, ms in per.items():
+        avg = sum(ms) / len(ms)
+        kind, work = algo.get(name, ("hbm", 0))
+        if kind == "tensor":
+            ach = work / (avg * 1e-3) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            unit = "TFLOP/s"
+        else:
+            ach = work / (avg * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        kernels[name] = {"launches": len(ms), "avg_ms": avg, "total_ms": sum(ms), "bound": kind,
+                         "achieved": ach, "unit": unit, "frac": ach / peak}
+    dominant = max(kernels, key=lambda n: kernels[n]["total_ms"])
+    dk_ = kernels[dominant]
+    roofline = {
+        "kernel": dominant, "bound": dk_["bound"], "achieved": dk_["achieved"],
+        "peak": peaks["bf16_tflops_sustained"] if dk_["bound"] == "tensor" else peaks["hbm_gbs"],
+        "unit": dk_["unit"], "frac": dk_["frac"],
+        "traffic": ncu_traffic(dominant, w.name),
+        "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if dk_['bound'] == 'tensor' else 'hbm_gbs'})",
+    }
+    if dk_["bound"] == "tensor":
+        roofline["frac_of_burst_peak"] = dk_["achieved"] / peaks["bf16_tflops"]
+
+    # ---------------- end to end through the public API with host buffers
+    pin = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
+           (("q", q), ("k", k), ("v", v), ("z", z), ("dO", dO))}
+    for n, t in (("q", q), ("k", k), ("v", v), ("z", z), ("dO", dO)):
+        pin[n].copy_(t)
+    outs = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
+            (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dz", dz))}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def e2e_step():
+        for n, t in (("q", q), ("k", k), ("v", v), ("z", z), ("dO", dO)):
+            t.copy_(pin[n], non_blocking=True)
+        step()
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dz", dz)):
+            outs[n].copy_(t, non_blocking=True)
+        torch.cuda.synchronize()  # the host reads the results
+
+    e2e_step()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * flops_step * args.steps / e2e_s / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, dt_cpu = oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle", "sample": sample_desc(),
+               "seconds": dt_cpu}
+
+    if rank == 0:
+        fwd_ms = sum(kernels[n]["total_ms"] for n in kernels if n in ("attn_fwd",)) / args.steps
+        bwd_ms = sum(kernels[n]["total_ms"] for n in kernels if n == "attn_bwd") / args.steps
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(world),
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": len(records),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "breakdown": {
+                "step_ms_median": statistics.median(step_ms),
+                "fwd_attn_ms": fwd_ms, "fwd_attn_tflops": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
+                "bwd_attn_ms": bwd_ms, "bwd_attn_tflops": w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
+                "kernels": kernels,
+            },
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("fox", "reference"), default="fox")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_fox(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+// C ABI of libfox.so: argument validation, workspace layout, TMA descriptor
+// construction and kernel launches. See include/fox.h for the contract.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fox.h"
+#include "fox_internal.h"
+
+namespace fox {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ tracing
+namespace {
+struct TraceRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace_pool;  // events are created once and reused
+size_t g_trace_used = 0;
+}  // namespace
+
+bool trace_enabled() {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  return g_trace_on;
+}
+
+TraceScope::TraceScope(const char* name, cudaStream_t s) : stream(s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) return;
+  if (g_trace_used == g_trace_pool.size()) {
+    TraceRec r{name, nullptr, nullptr};
+    if (cudaEventCreate(&r.start) != cudaSuccess) return;
+    if (cudaEventCreate(&r.stop) != cudaSuccess) {
+      cudaEventDestroy(r.start);
+      return;
+    }
+    g_trace_pool.push_back(r);
+  }
+  slot = static_cast<int>(g_trace_used++);
+  g_trace_pool[slot].name = name;
+  cudaEventRecord(g_trace_pool[slot].start, s);
+}
+
+TraceScope::~TraceScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  cudaEventRecord(g_trace_pool[slot].stop, stream);
+}
+
+}  // namespace fox
+
+using namespace fox;
+
+namespace {
+
+constexpr long long kMaxTokens = (1LL << 31) - 1;
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Shape/flag checks shared by both directions. Pointers are checked separately.
+fox_status check_params(const fox_params* p) {
+  if (!p) return FOX_ERR_INVALID_ARG;
+  if (p->B < 0 || p->N < 0 || p->H < 0 || p->d <= 0) return FOX_ERR_INVALID_ARG;
+  if (p->dtype != FOX_DTYPE_BF16 && p->dtype != FOX_DTYPE_F32) return FOX_ERR_INVALID_ARG;
+  if (p->bias_from_j != 0 && p->bias_from_j != 1) return FOX_ERR_INVALID_ARG;
+  if (!(p->scale >= 0.f) || std::isinf(p->scale)) return FOX_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return FOX_ERR_UNSUPPORTED;
+  const long long BH = (long long)p->B * p->H;
+  if (BH > kMaxTokens || (long long)p->N > kMaxTokens - 2 * kTile) return FOX_ERR_INVALID_ARG;
+  if (BH * (long long)p->N > kMaxTokens) return FOX_ERR_INVALID_ARG;
+  return FOX_OK;
+}
+
+float effective_scale(const fox_params* p) { return p->scale == 0.f ? 1.f / std::sqrt((float)p->d) : p->scale; }
+
+bool empty_problem(const fox_params* p) { return p->B == 0 || p->H == 0 || p->N == 0; }
+
+fox_status check_workspace(void* ws, size_t bytes, size_t need) {
+  if (!ws || !aligned(ws, 256) || bytes < need) return FOX_ERR_WORKSPACE;
+  return FOX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fox_version(void) { return 100; }
+
+const char* fox_status_string(fox_status s) {
+  switch (s) {
+    case FOX_OK: return "FOX_OK";
+    case FOX_ERR_INVALID_ARG: return "FOX_ERR_INVALID_ARG: invalid argument (null pointer, size, alignment or flag)";
+    case FOX_ERR_UNSUPPORTED: return "FOX_ERR_UNSUPPORTED: head dimension or dtype not implemented";
+    case FOX_ERR_WORKSPACE: return "FOX_ERR_WORKSPACE: workspace null, misaligned or too small";
+    case FOX_ERR_CUDA: return "FOX_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FOX_ERR_TIMEOUT: return "FOX_ERR_TIMEOUT: a device-side wait gave up";
+    case FOX_ERR_DEVICE: return "FOX_ERR_DEVICE: device-side error bit set";
+  }
+  return "FOX_ERR_UNKNOWN";
+}
+
+size_t fox_fwd_workspace_bytes(const fox_params* p) {
+  if (check_params(p) != FOX_OK) return 0;
+  return gate_layout(p->B, p->N, p->H).end;
+}
+
+size_t fox_bwd_workspace_bytes(const fox_params* p) {
+  if (check_params(p) != FOX_OK) return 0;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  return bwd_layout(g, p->d).end;
+}
+
+fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (empty_problem(p)) return FOX_OK;
+  if (!q || !k || !v || !z || !o || !lse) return FOX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(z, 4) ||
+      !aligned(lse, 4))
+    return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  st = check_workspace(workspace, workspace_bytes, g.end);
+  if (st != FOX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+
+  char* ws = static_cast<char*>(workspace);
+  AttnFwdArgs a;
+  a.B = p->B;
+  a.N = p->N;
+  a.H = p->H;
+  a.d = p->d;
+  a.scale = effective_scale(p);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.rowloc = reinterpret_cast<const float*>(ws + g.rowloc);
+  a.colrec = reinterpret_cast<const float*>(ws + g.colrec);
+  a.err = reinterpret_cast<uint32_t*>(ws);
+  if (p->dtype == FOX_DTYPE_F32) {
+    if (p->B * p->H > 65535) return FOX_ERR_UNSUPPORTED;
+    return launch_attn_fwd_f32(a, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
+  }
+  CUtensorMap maps[3];
+  if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d) ||
+      !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d))
+    return FOX_ERR_CUDA;
+  return launch_attn_fwd_bf16(a, maps, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
+}
+
+fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,
+                   const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dz, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (p->dtype != FOX_DTYPE_BF16) return FOX_ERR_UNSUPPORTED;
+  if (empty_problem(p)) return FOX_OK;
+  if (!q || !k || !v || !z || !o || !lse || !dO || !dq || !dk || !dv || !dz) return FOX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(z, 4) || !aligned(lse, 4) ||
+      !aligned(dz, 4))
+    return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  const BwdLayout w = bwd_layout(g, p->d);
+  st = check_workspace(workspace, workspace_bytes, w.end);
+  if (st != FOX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  CUtensorMap maps[4];
+  if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d) ||
+      !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[3], dO, p->B, p->N, p->H, p->d))
+    return FOX_ERR_CUDA;
+  AttnBwdArgs a;
+  a.B = p->B;
+  a.N = p->N;
+  a.H = p->H;
+  a.d = p->d;
+  a.bias_from_j = p->bias_from_j;
+  a.scale = effective_scale(p);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.z = z;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dz = dz;
+  a.ws = static_cast<char*>(workspace);
+  return launch_attn_bwd(a, g, w, maps, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
+}
+
+fox_status fox_trace_begin(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = true;
+  g_trace_used = 0;
+  return FOX_OK;
+}
+
+int fox_trace_end(fox_trace_record* out, int max_records) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  const int n = static_cast<int>(g_trace_used);
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(g_trace_pool[i].stop) != cudaSuccess) return -1;
+    if (out && i < max_records) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, g_trace_pool[i].start, g_trace_pool[i].stop) != cudaSuccess) return -1;
+      out[i].kernel = g_trace_pool[i].name;
+      out[i].ms = ms;
+    }
+  }
+  g_trace_used = 0;
+  return n;
+}
+
+fox_status fox_check_error(void* workspace, void* stream) {
+  if (!workspace || !aligned(workspace, 256)) return FOX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FOX_ERR_CUDA;
+  if (word == 0) return FOX_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return FOX_ERR_CUDA;
+  const uint32_t timeout_bits = 0x7u;
+  return (word & timeout_bits) ? FOX_ERR_TIMEOUT : FOX_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,459 @@
+// Fused causal forget-gated attention forward, bf16 in / fp32 accumulate, for
+// sm_103a: TMA-staged Q/K/V tiles, S = Q K^T and O += P V as tcgen05 MMAs
+// into tensor memory, the forget bias and causal mask folded into an online
+// softmax in registers, fully masked tiles never visited.
+//
+// Math ("Forgetting Transformer (FoX) Attention" module source,
+// ForgettingAttention.forward; foxwindow README, score form): for query row i
+// and key j <= i,  x_ij = scale * q_i.k_j + c_i - c_j  (j+1 convention; the j
+// convention swaps the column term for c_{j-1}), O_i = softmax_j(x_ij) V.
+// In log2 units with the two-level gate terms (see fox_internal.h):
+//   x_ij * log2e = l_i + [ scale*log2e * S_ij - kappa_j ] + (base_I - base_J).
+// The row term l_i is constant along the row and cancels in the softmax; it
+// is added back into LSE only.
+//
+// KV tiles are visited from the diagonal backwards. The forget bias falls
+// monotonically with distance (foxwindow README, "The window is a
+// first-passage time"), so the row maximum is almost always found in the
+// first tile; later tiles then take a single pass with that maximum, and the
+// rare tile whose maximum exceeds it by more than 2^8 is recomputed after
+// rescaling O.
+//
+// CTA = one (b, h) and a block of 256 query rows = two 128-row Q tiles that
+// share every K/V tile (ping-pong: while the softmax of one tile runs, the
+// tensor core works on the other). Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue of Q tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax + epilogue of Q tile 1
+//   warp  8    TMA producer (Q once; K, V and the column-term record per KV tile, 2 stages)
+//   warp  9    TMEM allocator and single-thread MMA issuer
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
+// P (bf16) overwrites the first 64 columns of its S buffer and feeds the P V
+// MMA straight from tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fox_internal.h"
+#include "fox_ptx.cuh"
+
+namespace fox {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kKappaBytes = kColRec * 4;   // 528
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum while the tile max stays within 2^8
+
+struct FwdKParams {
+  int B, N, H, nT, nQB, Npad;
+  float scale2;  // scale * log2 e
+  const float* rowloc;
+  const float* colrec;
+  __nv_bfloat16* o;
+  float* lse;
+  uint32_t* err;
+};
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTileBytes;
+  static constexpr int kK = 2 * kTileBytes;
+  static constexpr int kV = 4 * kTileBytes;
+  static constexpr int kKappa = 6 * kTileBytes;
+  static constexpr int kBars = kKappa + 2 * kKappaBytes;  // 8-byte aligned (528 * 2 = 1056)
+  static constexpr int kNumBars = 16;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  // Slack for 1024-byte alignment of the base; at least 116 KB so that only one CTA (which
+  // takes all 512 TMEM columns) is ever resident per SM.
+  static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
+};
+
+enum Bar {
+  B_Q = 0,
+  B_KFULL = 1,    // +stage
+  B_KEMPTY = 3,   // +stage
+  B_VFULL = 5,    // +stage
+  B_VEMPTY = 7,   // +stage
+  B_SFULL = 9,    // +tile
+  B_PFULL = 11,   // +tile
+  B_OFINAL = 13,  // +tile
+  B_DONE = 15,
+};
+
+// Row maximum of t_j = scale2 * S_j - kappa_j over the 128 columns of this
+// thread's S row in tensor memory (columns j > r masked on the diagonal tile).
+template <bool kDiag>
+__device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float scale2, int r) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int qt = 0; qt < 4; ++qt) {
+    uint32_t raw[32];
+    tmem_ld32(tS + 32 * qt, raw);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const int j = 32 * qt + 4 * j4;
+      const float4 kk = lds_f4(kap + j);
+      float t[4];
+      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
+      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
+      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
+      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
+      if (kDiag) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e > r) t[e] = -INFINITY;
+      }
+      m0 = fmaxf(m0, fmaxf(t[0], t[2]));
+      m1 = fmaxf(m1, fmaxf(t[1], t[3]));
+    }
+  }
+  return fmaxf(m0, m1);
+}
+
+// p_j = 2^(t_j - off) for the 128 columns, written back as bf16 pairs into
+// the first 64 columns of the same S row (chunk q's P lands on columns
+// [16q, 16q+16), which only hold S values already read). Returns sum_j p_j (fp32).
+template <bool kDiag>
+__device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float scale2, float off, int r) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int qt = 0; qt < 4; ++qt) {
+    uint32_t raw[32];
+    tmem_ld32(tS + 32 * qt, raw);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const int j = 32 * qt + 4 * j4;
+      const float4 kk = lds_f4(kap + j);
+      float t[4];
+      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
+      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
+      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
+      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
+      if (kDiag) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e > r) t[e] = -INFINITY;
+      }
+      float pr[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[e] = ex2_approx(t[e] - off);
+      s0 += pr[0] + pr[2];
+      s1 += pr[1] + pr[3];
+      pk[2 * j4] = pack_bf16x2(pr[0], pr[1]);
+      pk[2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
+    }
+    tmem_st16(tS + 16 * qt, pk);
+  }
+  return s0 + s1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const FwdKParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int qb = p.nQB - 1 - static_cast<int>(blockIdx.x) / BH;  // longest causal rows first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  // Q tile k covers rows [128*I_k, 128*I_k + 128). KV tiles are streamed in
+  // sequence order s = 0, 1, ..., nJ-1 with J = Jtop - s; tile k takes part
+  // for s >= first_k (its own diagonal tile is s = first_k).
+  const int I0 = 2 * qb, I1 = 2 * qb + 1;
+  const bool has1 = I1 < p.nT;
+  const int Jtop = has1 ? I1 : I0;
+  const int nJ = Jtop + 1;
+  const int first0 = has1 ? 1 : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_Q], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[B_KFULL + s], 1);
+      mbar_init(&bars[B_KEMPTY + s], 1);
+      mbar_init(&bars[B_VFULL + s], 1);
+      mbar_init(&bars[B_VEMPTY + s], 1);
+      mbar_init(&bars[B_SFULL + s], 1);
+      mbar_init(&bars[B_PFULL + s], 128);
+      mbar_init(&bars[B_OFINAL + s], 1);
+    }
+    mbar_init(&bars[B_DONE], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+      constexpr uint32_t tb = L::kTileBytes;
+      mbar_arrive_expect_tx(&bars[B_Q], has1 ? 2 * tb : tb);
+      for (int x = 0; x < D / 64; ++x) {
+        tma_load_4d(sm + L::kQ0 + x * 16384, &tmap_q, &bars[B_Q], x * 64, h, I0 * kTile, b);
+        if (has1) tma_load_4d(sm + L::kQ1 + x * 16384, &tmap_q, &bars[B_Q], x * 64, h, I1 * kTile, b);
+      }
+      const float* rec_base = p.colrec + (size_t)bh * p.nT * kColRec;
+      int fills[2] = {0, 0};  // fills issued per stage (K and V of a stage go in lock step)
+      for (int s = 0; s < nJ; ++s) {
+        const int st = s & 1, n = s >> 1, J = Jtop - s;
+        if (n > 0 && !mbar_wait(&bars[B_KEMPTY + st], (n - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC)) break;
+        mbar_arrive_expect_tx(&bars[B_KFULL + st], tb);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_4d(sm + L::kK + st * tb + x * 16384, &tmap_k, &bars[B_KFULL + st], x * 64, h, J * kTile, b);
+        if (n > 0 && !mbar_wait(&bars[B_VEMPTY + st], (n - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC)) {
+          mbar_wait_drain(&bars[B_KFULL + st], n & 1);  // the K copy of this fill is in flight
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[B_VFULL + st], tb + kKappaBytes);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_4d(sm + L::kV + st * tb + x * 16384, &tmap_v, &bars[B_VFULL + st], x * 64, h, J * kTile, b);
+        bulk_load(sm + L::kKappa + st * kKappaBytes, rec_base + (size_t)J * kColRec, kKappaBytes,
+                  &bars[B_VFULL + st]);
+        ++fills[st];
+      }
+      // Drain: every copy this CTA issued must land before shared memory is released.
+      mbar_wait_drain(&bars[B_Q], 0);
+      for (int st = 0; st < 2; ++st) {
+        if (fills[st] == 0) continue;
+        mbar_wait_drain(&bars[B_KFULL + st], (fills[st] - 1) & 1);
+        mbar_wait_drain(&bars[B_VFULL + st], (fills[st] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t tb = L::kTileBytes;
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      const uint32_t tS[2] = {tbase, tbase + 128};
+      const uint32_t tO[2] = {tbase + 256, tbase + 256 + D};
+      const uint32_t sQ[2] = {smem_u32(sm + L::kQ0), smem_u32(sm + L::kQ1)};
+      const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+      const int first[2] = {first0, 0};
+      const bool active[2] = {true, has1};
+      auto issue_s = [&](int k, int st) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          umma_ss(tS[k], sdesc_sw128(sQ[k] + off, 16, 1024), sdesc_sw128(sK + st * tb + off, 16, 1024), idS,
+                  ks > 0);
+        }
+      };
+      auto issue_pv = [&](int k, int st, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          umma_ts(tO[k], tS[k] + ks * 8, sdesc_sw128(sV + st * tb + ks * 2048, 16384, 1024), idO,
+                  (acc || ks > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
+                mbar_wait(&bars[B_KFULL + 0], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+      if (ok) {
+        tc_fence_after();
+        for (int k = 0; k < 2; ++k)
+          if (active[k] && first[k] == 0) {
+            issue_s(k, 0);
+            umma_commit(&bars[B_SFULL + k]);
+          }
+        umma_commit(&bars[B_KEMPTY + 0]);
+      }
+      for (int s = 0; s < nJ && ok; ++s) {
+        const int st = s & 1, nst = (s + 1) & 1;
+        bool kready = false;
+        auto wait_next_k = [&]() -> bool {
+          if (!kready) {
+            if (!mbar_wait(&bars[B_KFULL + nst], ((s + 1) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA))
+              return false;
+            tc_fence_after();
+            kready = true;
+          }
+          return true;
+        };
+        ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+        for (int k = 0; k < 2 && ok; ++k) {
+          if (!active[k]) continue;
+          if (s >= first[k]) {
+            ok = mbar_wait(&bars[B_PFULL + k], (s - first[k]) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(k, st, s > first[k]);
+            if (s + 1 < nJ) {
+              if (!(ok = wait_next_k())) break;
+              issue_s(k, nst);
+              umma_commit(&bars[B_SFULL + k]);
+            } else {
+              umma_commit(&bars[B_OFINAL + k]);
+            }
+          } else if (s + 1 == first[k]) {
+            if (!(ok = wait_next_k())) break;
+            issue_s(k, nst);
+            umma_commit(&bars[B_SFULL + k]);
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bars[B_VEMPTY + st]);
+        if (kready) umma_commit(&bars[B_KEMPTY + nst]);
+      }
+      // Every MMA issued above must retire before tensor memory is freed.
+      umma_commit(&bars[B_DONE]);
+      mbar_wait_drain(&bars[B_DONE], 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ softmax / epilogue
+    const int k = warp >> 2;        // Q tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quarter
+    const int r = wq * 32 + lane;   // row within the Q tile
+    const int I = k ? I1 : I0;
+    const int first = k ? 0 : first0;
+    const int nJk = (k == 1 && !has1) ? 0 : I + 1;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + k * 128 + lane_off;
+    const uint32_t tO = tbase + 256 + k * D + lane_off;
+    const int i = I * kTile + r;
+    if (nJk > 0) {
+      const float* recI = p.colrec + ((size_t)bh * p.nT + I) * kColRec;
+      const float baseI_hi = recI[kTile], baseI_lo = recI[kTile + 1];
+      const float row_term = p.rowloc[(size_t)bh * p.Npad + i];
+      float m_used = -INFINITY, l_sum = 0.f;
+      bool ok = true;
+      // Diagonal tile first (u = 0; base_I - base_J = 0 there).
+      ok = mbar_wait(&bars[B_SFULL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
+           mbar_wait(&bars[B_VFULL + (first & 1)], (first >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+      ok = __all_sync(0xffffffffu, ok);  // the tcgen05 loads below are warp-collective
+      if (ok) {
+        tc_fence_after();
+        const float* kap = reinterpret_cast<const float*>(sm + L::kKappa + (first & 1) * kKappaBytes);
+        m_used = row_max<true>(tS, kap, p.scale2, r);
+        l_sum = exp_pass<true>(tS, kap, p.scale2, m_used, r);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[B_PFULL + k]);
+      }
+      for (int u = 1; u < nJk && ok; ++u) {
+        const int s = first + u, st = s & 1;
+        ok = mbar_wait(&bars[B_SFULL + k], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
+             mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float* kap = reinterpret_cast<const float*>(sm + L::kKappa + st * kKappaBytes);
+        const float beta = (baseI_hi - kap[kTile]) + (baseI_lo - kap[kTile + 1]);
+        const float m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
+        const bool grow = m_cand > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          // Some row's maximum grew by more than 2^8: rescale O and l of those rows
+          // (alpha = 1 for the others; the TMEM loads/stores are warp-collective, so
+          // the whole warp takes this branch). s_full of this tile was committed after
+          // the previous P V, so O is settled.
+          const float alpha = grow ? ex2_approx(m_used - m_cand) : 1.f;
+          l_sum *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c, o);
+          }
+          if (grow) m_used = m_cand;
+        }
+        l_sum += exp_pass<false>(tS, kap, p.scale2, m_used - beta, r);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[B_PFULL + k]);
+      }
+      if (ok) ok = mbar_wait(&bars[B_OFINAL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l_sum;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait();
+          if (i < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + (((size_t)b * p.N + i) * p.H + h) * D + c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+              dst[q4] = w;
+            }
+          }
+        }
+        if (i < p.N) p.lse[((size_t)b * p.N + i) * p.H + h] = (m_used + __log2f(l_sum) + row_term) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
+  using L = FwdLayout<D>;
+  static_assert(L::kAlloc <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fox_attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  FwdKParams p;
+  p.B = a.B;
+  p.N = a.N;
+  p.H = a.H;
+  p.nT = nT;
+  p.nQB = (nT + 1) / 2;
+  p.Npad = Npad;
+  p.scale2 = a.scale * kLog2e;
+  p.rowloc = a.rowloc;
+  p.colrec = a.colrec;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.err = a.err;
+  const long long blocks = (long long)p.nQB * a.B * a.H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  {
+    TraceScope trace("attn_fwd", s);
+    fox_attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
+  if (a.d == 64) return launch_d<64>(a, maps, nT, Npad, s);
+  if (a.d == 128) return launch_d<128>(a, maps, nT, Npad, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fox

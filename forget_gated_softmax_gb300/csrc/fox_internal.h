@@ -1,0 +1,132 @@
+// Internal layout and launcher declarations shared by the library's
+// translation units (host side and kernels). Not part of the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+namespace fox {
+
+constexpr int kTile = 128;          // tokens per sequence tile (MMA M and KV tile)
+constexpr int kColRec = kTile + 4;  // floats per column record: 128 column terms + base hi, base lo, 2 pad
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Gate terms the attention kernels read, all in log2 units (natural value * log2 e).
+//   rowloc[bh][t]   l_t  = sum_{l = 128*T .. t} a_l          (T = t / 128; inclusive, tile-local)
+//   colrec[bh][T]   { kappa_j for j in tile T (tile-local column term:
+//                     inclusive for the j+1 convention, exclusive for the j convention),
+//                     base_T hi, base_T lo, 0, 0 },  base_T = sum_{l < 128*T} a_l (fp64 scan, split hi+lo)
+//   tiletot[bh][T]  sum of a over tile T (fp32, scratch between the two gate kernels)
+// so that, for i in tile I and j in tile J, D_ij * log2 e = l_i - kappa_j + (base_I - base_J).
+struct GateLayout {
+  int BH = 0, N = 0, nT = 0, Npad = 0;
+  size_t rowloc = 0, colrec = 0, tiletot = 0, end = 0;  // byte offsets from the workspace base
+};
+
+// Backward-only buffers that follow the gate buffers.
+struct BwdLayout {
+  size_t delta = 0;   // float [BH][Npad]   Delta_i = dO_i . O_i (0 past the sequence end)
+  size_t rho = 0;     // float [BH][Npad]   LSE_i * log2 e - l_i: row offset to recompute P (+inf past the end)
+  size_t colsum = 0;  // float [BH][Npad]   C_j = sum_i dS_ij
+  size_t dqacc = 0;   // float [BH][Npad][d] dQ accumulator (fp32, unscaled)
+  size_t end = 0;
+};
+
+constexpr size_t kErrWordBytes = 256;  // workspace header: uint32 error word + padding
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline GateLayout gate_layout(int B, int N, int H) {
+  GateLayout g;
+  g.BH = B * H;
+  g.N = N;
+  g.nT = (N + kTile - 1) / kTile;
+  g.Npad = g.nT * kTile;
+  size_t off = kErrWordBytes;
+  g.rowloc = off;
+  off = align_up(off + sizeof(float) * (size_t)g.BH * g.Npad, 256);
+  g.colrec = off;
+  off = align_up(off + sizeof(float) * (size_t)g.BH * g.nT * kColRec, 256);
+  g.tiletot = off;
+  off = align_up(off + sizeof(float) * (size_t)g.BH * g.nT, 256);
+  g.end = off;
+  return g;
+}
+
+inline BwdLayout bwd_layout(const GateLayout& g, int d) {
+  BwdLayout w;
+  size_t off = g.end;
+  const size_t row = sizeof(float) * (size_t)g.BH * g.Npad;
+  w.delta = off;
+  off = align_up(off + row, 256);
+  w.rho = off;
+  off = align_up(off + row, 256);
+  w.colsum = off;
+  off = align_up(off + row, 256);
+  w.dqacc = off;
+  off = align_up(off + row * (size_t)d, 256);
+  w.end = off;
+  return w;
+}
+
+// ---- kernel tracing (benchmark support) ----
+// While tracing is on, TraceScope brackets a launch with two CUDA events on
+// its stream; fox_trace_end() reports each launch's name and duration.
+bool trace_enabled();
+struct TraceScope {
+  int slot = -1;
+  cudaStream_t stream = nullptr;
+  TraceScope(const char* name, cudaStream_t s);
+  ~TraceScope();
+};
+
+// ---- launchers (return cudaGetLastError() of the launch) ----
+cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
+                             cudaStream_t s);
+
+struct AttnFwdArgs {
+  int B, N, H, d;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const float* rowloc;
+  const float* colrec;
+  uint32_t* err;
+};
+
+cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v */, int nT, int Npad,
+                                 cudaStream_t s);
+cudaError_t launch_attn_fwd_f32(const AttnFwdArgs& a, int nT, int Npad, cudaStream_t s);
+
+struct AttnBwdArgs {
+  int B, N, H, d, bias_from_j;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* z;
+  const void* o;
+  const float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dz;
+  char* ws;  // workspace base (gate layout, then the backward layout)
+};
+
+// Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ
+// conversion and the reverse gate scan; the gate scan must already be in ws.
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w,
+                            const CUtensorMap* maps /* q, k, v, dO */, cudaStream_t s);
+
+// Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 x 1 x 128 x 1 and 128-byte swizzle.
+// Returns false when the driver entry point is unavailable or encoding fails.
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d);
+
+}  // namespace fox

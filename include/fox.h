@@ -1,0 +1,134 @@
+/*
+ * fox.h — C ABI of the forget-gated causal softmax attention library (libfox.so).
+ *
+ * The operation (Forgetting Transformer, FoX). Per batch b and head h, with
+ * tokens t = 0..N-1:
+ *   f_t = sigmoid(z_t),  a_t = log f_t,  c_t = sum_{l<=t} a_l
+ *   D_ij = c_i - c_j          (bias_from_j = 0, the default; D_ii = 0)
+ *   D_ij = c_i - c_{j-1}      (bias_from_j = 1; c_{-1} = 0)
+ *   S_ij = scale * q_i . k_j + D_ij  for j <= i  (causal; j > i excluded)
+ *   LSE_i = ln sum_{j<=i} exp(S_ij),  O_i = sum_{j<=i} exp(S_ij - LSE_i) v_j
+ * Sources: "Forgetting Transformer (FoX) Attention" module source
+ * (frankenstein-transformer docs, fox_attn: module docstring formula and
+ * ForgettingAttention.forward — sigmoid gate, log, cumsum, outer difference,
+ * causal mask, scaled logits + bias, softmax, attn @ v); foxwindow README,
+ * "The window is a first-passage time" (score form with the sum from j+1);
+ * fast-transformers "Creating a custom attention layer", "New Attention"
+ * (attention-only call on projected, head-split inputs, [batch, length,
+ * heads, dim] layout). The backward is the chain rule through the same
+ * formula; the gate gradient is d a_t = sum_{s>=t} (R_s - C_s) (+ C_t under
+ * bias_from_j = 1), R/C the row/column sums of dS, and dz_t = d a_t * sigmoid(-z_t).
+ *
+ * Layout (all row-major, contiguous, device memory):
+ *   q, k, v, o, dO, dq, dk, dv : [B, N, H, d], element type per params.dtype
+ *   z, lse, dz                  : [B, N, H] fp32
+ * Alignment: q, k, v, o, dO, dq, dk, dv 16-byte aligned; z, lse, dz 4-byte
+ * aligned; workspace 256-byte aligned.
+ *
+ * Ownership and threading: the caller owns every buffer, the workspace
+ * included. The library allocates no device memory, keeps no state between
+ * calls except a lazily-resolved driver entry point, and never synchronises
+ * (fox_check_error excepted). All work is enqueued on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream) of the current device.
+ * Outputs are fully overwritten. Calls on different streams must use
+ * different workspaces.
+ *
+ * Errors: every call validates its arguments on the host and returns a
+ * fox_status without touching the GPU when they are wrong. Device-side waits
+ * are bounded; a wait that gives up sets a bit in the workspace's error word
+ * (reset by each fox_fwd / fox_bwd call) and the kernel exits cleanly;
+ * fox_check_error reports it.
+ */
+#ifndef FOX_H_
+#define FOX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fox_status {
+  FOX_OK = 0,
+  FOX_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, bad flag or dtype */
+  FOX_ERR_UNSUPPORTED = 2, /* well-formed but not implemented (d not in {64, 128}; fp32 backward) */
+  FOX_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than the size query */
+  FOX_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  FOX_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (from fox_check_error) */
+  FOX_ERR_DEVICE = 6       /* another device-side error bit was set (from fox_check_error) */
+} fox_status;
+
+enum { FOX_DTYPE_BF16 = 0, FOX_DTYPE_F32 = 1 };
+
+typedef struct fox_params {
+  int B;           /* batch size, >= 0 */
+  int N;           /* sequence length, >= 0 (any value; no multiple-of-tile requirement) */
+  int H;           /* heads, >= 0; q, k and v have the same head count */
+  int d;           /* head dimension: 64 or 128 */
+  int dtype;       /* FOX_DTYPE_BF16 (tensor cores) or FOX_DTYPE_F32 (forward only) */
+  float scale;     /* multiplies q.k only; 0 selects d^-1/2 (module __init__: head_dim ** -0.5) */
+  int bias_from_j; /* 0: D_ij = sum_{l=j+1}^{i} log f_l (module code, foxwindow); 1: sum_{l=j}^{i} (module docstring) */
+} fox_params;
+
+/* Workspace bytes fox_fwd / fox_bwd need for these params (0 if params are invalid). */
+size_t fox_fwd_workspace_bytes(const fox_params* p);
+size_t fox_bwd_workspace_bytes(const fox_params* p);
+
+/*
+ * Forward. Reads q, k, v [B,N,H,d] and gate logits z [B,N,H] (fp32; +inf
+ * allowed and means f = 1; -inf and NaN are outside the domain). Writes
+ * O [B,N,H,d] (params.dtype; bf16 rounded to nearest even) and
+ * LSE [B,N,H] (fp32, natural log, bias included).
+ * Steps: gate log-sigmoid + per-head prefix scan into the workspace, then the
+ * fused causal attention kernel. B*H == 0 or N == 0 returns FOX_OK with no work.
+ */
+fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward (bf16 only). Reads q, k, v, z, the forward's O and LSE, and the
+ * upstream gradient dO; writes dq, dk, dv [B,N,H,d] bf16 and dz [B,N,H] fp32.
+ * Steps: gate scan, Delta_i = dO_i . O_i, the fused recompute-and-backward
+ * attention kernel (dK, dV, dQ accumulator and the column sums of dS), the
+ * dQ conversion and the reverse gate scan.
+ */
+fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,
+                   const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dz, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device error word of
+ * `workspace` (the one passed to the last fox_fwd / fox_bwd on it).
+ * Returns FOX_OK, FOX_ERR_TIMEOUT or FOX_ERR_DEVICE, or FOX_ERR_CUDA if the
+ * stream itself reports an error.
+ */
+fox_status fox_check_error(void* workspace, void* stream);
+
+/*
+ * Kernel-level timing, for benchmarks. Between fox_trace_begin() and
+ * fox_trace_end(), every kernel launch this library enqueues (from any host
+ * thread) is bracketed by two CUDA events recorded on its stream; events are
+ * created on first use and reused. fox_trace_end() stops recording, waits for
+ * the recorded events, writes up to max_records {kernel name, milliseconds}
+ * in launch order into `out` (may be NULL), and returns the number of
+ * launches recorded, or -1 if a CUDA event call failed. Names are static strings.
+ */
+typedef struct fox_trace_record {
+  const char* kernel;
+  float ms;
+} fox_trace_record;
+fox_status fox_trace_begin(void);
+int fox_trace_end(fox_trace_record* out, int max_records);
+
+/* Static string naming a status. */
+const char* fox_status_string(fox_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int fox_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOX_H_ */

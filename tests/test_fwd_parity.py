@@ -1,0 +1,159 @@
+"""Forward parity: the CUDA path (through the C ABI) against the CPU fp64
+oracle on the same seeded inputs, element by element.
+
+Small cases span several 128-row tiles and ragged tails and are compared in
+full; the named full-size workloads are compared on all heads at sampled
+rows (each sampled output computed on its own by the oracle)."""
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import fox_oracle as ora
+
+from foxtest import (TOL_LSE_BF16, TOL_LSE_F32, TOL_O_BF16, TOL_O_F32, exact, o_excess_error, sample_rows,
+                     tensor_f64, to_torch)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import forget_gated_softmax_gb300 as fox
+
+    fox.lib()  # fails loudly if the library is missing
+
+
+def run_fwd(w: wl.Workload, scale=0.0, arrays=None):
+    import forget_gated_softmax_gb300 as fox
+
+    arrays = arrays if arrays is not None else wl.draw(w, with_dO=False)
+    t = to_torch(arrays, w.dtype)
+    ws = fox.workspace(fox.fox_fwd_workspace_bytes(fox.make_params(w.B, w.N, w.H, w.d, 0 if w.dtype == "bf16" else 1,
+                                                                   scale, w.bias_from_j)), "cuda")
+    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], scale=scale, bias_from_j=w.bias_from_j, ws=ws)
+    assert fox.fox_check_error(ws) == 0
+    torch.cuda.synchronize()
+    return arrays, o, lse
+
+
+def check_full(w: wl.Workload, scale=0.0, arrays=None):
+    arrays, o, lse = run_fwd(w, scale, arrays)
+    x = exact(arrays, w.dtype)
+    O_ref, L_ref = ora.forward(x["q"], x["k"], x["v"], x["z"], scale=scale or None, bias_from_j=w.bias_from_j)
+    tol_o, tol_l = (TOL_O_BF16, TOL_LSE_BF16) if w.dtype == "bf16" else (TOL_O_F32, TOL_LSE_F32)
+    err_o = o_excess_error(tensor_f64(o), O_ref, w.dtype)
+    err_l = np.abs(tensor_f64(lse) - L_ref).max()
+    assert np.isfinite(tensor_f64(o)).all() and np.isfinite(tensor_f64(lse)).all()
+    assert err_o <= tol_o, (w.name, "O", err_o)
+    assert err_l <= tol_l, (w.name, "LSE", err_l)
+    return err_o, err_l
+
+
+def check_rows(w: wl.Workload, rows_per_head=24, heads=None, seed=0):
+    arrays, o, lse = run_fwd(w)
+    x = exact(arrays, w.dtype)
+    O = tensor_f64(o)
+    L = tensor_f64(lse)
+    worst_o = worst_l = 0.0
+    heads = heads if heads is not None else [(b, h) for b in range(w.B) for h in range(w.H)]
+    for n, (b, h) in enumerate(heads):
+        rows = sample_rows(w.N, rows_per_head, seed + n)
+        Or, Lr = ora.attention_rows(x["q"][b, :, h], x["k"][b, :, h], x["v"][b, :, h], x["z"][b, :, h], rows,
+                                    bias_from_j=w.bias_from_j)
+        worst_o = max(worst_o, o_excess_error(O[b, rows, h], Or, w.dtype))
+        worst_l = max(worst_l, np.abs(L[b, rows, h] - Lr).max())
+    assert worst_o <= TOL_O_BF16, (w.name, "O", worst_o)
+    assert worst_l <= TOL_LSE_BF16, (w.name, "LSE", worst_l)
+    return worst_o, worst_l
+
+
+SMALL = [
+    (1, 1, 1, 64),
+    (1, 2, 2, 64),
+    (2, 127, 3, 64),
+    (1, 128, 2, 128),
+    (2, 129, 2, 128),
+    (1, 255, 1, 64),
+    (1, 256, 2, 128),
+    (2, 300, 3, 128),
+    (1, 513, 2, 64),
+    (1, 1000, 2, 128),
+]
+
+
+@pytest.mark.parametrize("B,N,H,d", SMALL)
+@pytest.mark.parametrize("from_j", [False, True])
+def test_small_shapes_bf16(B, N, H, d, from_j):
+    w = wl.Workload(f"s{B}x{N}x{H}x{d}", B, N, H, d, "bf16", seed=N * 7 + d, gate="head_uniform", lo=-1.0,
+                    hi=5.0, bias_from_j=from_j)
+    check_full(w)
+
+
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+def test_custom_scale(scale):
+    w = wl.Workload("scale", 1, 300, 2, 64, "bf16", seed=11, gate="normal", lo=1.0)
+    check_full(w, scale=scale)
+
+
+def test_open_gate_and_closing_gates():
+    w = wl.Workload("open", 1, 384, 2, 128, "bf16", seed=5, gate="open")
+    check_full(w)
+    w2 = wl.Workload("fast", 1, 384, 2, 128, "bf16", seed=6, gate="normal", lo=-30.0, sigma=1.0)
+    check_full(w2)
+
+
+@pytest.mark.parametrize("B,N,H,d", [(1, 256, 2, 64), (1, 300, 3, 128), (2, 129, 1, 64)])
+def test_fp32_path(B, N, H, d):
+    w = wl.Workload("f32", B, N, H, d, "f32", seed=3, gate="normal", lo=2.0)
+    check_full(w)
+
+
+def test_tiny_f32_workload():
+    check_full(wl.TINY_F32)
+
+
+def test_mid_bf16_workload_full():
+    check_full(wl.MID_BF16)
+
+
+def test_long_bf16_workload_sampled_rows():
+    check_rows(wl.LONG_BF16, rows_per_head=20)
+
+
+@pytest.mark.parametrize("w", [wl.ALIBI_BF16, wl.OPEN_BF16], ids=["alibi", "open"])
+def test_limit_workloads_sampled_rows(w):
+    check_rows(w, rows_per_head=24)
+
+
+def test_train_workload_forward_sampled_rows():
+    check_rows(wl.TRAIN_BF16, rows_per_head=8)
+
+
+def test_forward_is_deterministic():
+    w = wl.Workload("det", 2, 700, 3, 128, "bf16", seed=9, gate="head_uniform", lo=0.0, hi=4.0)
+    a, o1, l1 = run_fwd(w)
+    _, o2, l2 = run_fwd(w, arrays=a)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_outputs_leave_neighbours_untouched():
+    """Guard bands around O and LSE keep their NaN fill: no write past the ends."""
+    import forget_gated_softmax_gb300 as fox
+
+    w = wl.Workload("guard", 1, 200, 3, 64, "bf16", seed=2, gate="normal", lo=1.0)
+    arrays = wl.draw(w)
+    t = to_torch(arrays, "bf16")
+    G = 4096
+    obuf = torch.full((G + w.B * w.N * w.H * w.d + G,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((G + w.B * w.N * w.H + G,), float("nan"), dtype=torch.float32, device="cuda")
+    o = obuf[G : G + w.B * w.N * w.H * w.d].view(w.B, w.N, w.H, w.d)
+    lse = lbuf[G : G + w.B * w.N * w.H].view(w.B, w.N, w.H)
+    fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(obuf[:G]).all() and torch.isnan(obuf[-G:]).all()
+    assert torch.isnan(lbuf[:G]).all() and torch.isnan(lbuf[-G:]).all()
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()

@@ -63,3 +63,11 @@ def test_named_workload_shapes():
     assert (wl.LONG_BF16.B, wl.LONG_BF16.H, wl.LONG_BF16.N, wl.LONG_BF16.d) == (1, 32, 16384, 128)
     assert wl.LONG_BF16.fwd_flops() == 2 * 32 * 16384**2 * 128
     assert wl.TRAIN_BF16.backward and wl.TRAIN_BF16.bwd_flops() == 2.5 * wl.TRAIN_BF16.fwd_flops()
+
+
+def test_native_generator_matches_numpy_definition():
+    u = np.empty(64, dtype=np.uint64)
+    wl._native().sm64_fill(11, 1000, 64, u.ctypes.data)
+    np.testing.assert_array_equal(u, wl.splitmix64(11, 1000, 64))
+    for start, count in ((0, 1), (6, 100001), (1 << 33, 4097)):
+        np.testing.assert_array_equal(wl.normals_f32(9, start, count), wl.normals(9, start, count).astype(np.float32))

@@ -19,8 +19,11 @@ does not change the other tensors.
 """
 from __future__ import annotations
 
+import ctypes
 import dataclasses
 import math
+import os
+import subprocess
 from typing import Optional
 
 import numpy as np
@@ -62,6 +65,38 @@ def normals(seed: int, start: int, count: int) -> np.ndarray:
         n = min(count - done, pair.size)
         out[done : done + n] = pair[:n]
         done += n
+    return out
+
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_CLIB_PATH = os.path.join(_HERE, "_gen.so")
+_clib = None
+
+
+def _native():
+    """The C version of the same generator (workloads/_gen.c), built with gcc on first use."""
+    global _clib
+    if _clib is None:
+        src = os.path.join(_HERE, "_gen.c")
+        if not os.path.exists(_CLIB_PATH) or os.path.getmtime(_CLIB_PATH) < os.path.getmtime(src):
+            tmp = _CLIB_PATH + f".{os.getpid()}.tmp"
+            subprocess.run(["gcc", "-O2", "-shared", "-fPIC", "-o", tmp, src, "-lm", "-lpthread"], check=True)
+            os.replace(tmp, _CLIB_PATH)
+        lib = ctypes.CDLL(_CLIB_PATH)
+        lib.sm64_normals_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_int]
+        lib.sm64_normals_f32.restype = None
+        lib.sm64_fill.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
+        lib.sm64_fill.restype = None
+        _clib = lib
+    return _clib
+
+
+def normals_f32(seed: int, start: int, count: int) -> np.ndarray:
+    """`count` standard normals rounded to fp32, from stream output `start` (C, all cores)."""
+    out = np.empty(count, dtype=np.float32)
+    if count:
+        _native().sm64_normals_f32(seed & 0xFFFFFFFFFFFFFFFF, start, count, out.ctypes.data, os.cpu_count() or 1)
     return out
 
 
@@ -140,7 +175,7 @@ def gate_logits(w: Workload) -> np.ndarray:
         m = 2.0 ** (-8.0 * (h + 1.0) / w.H)
         zh = (-np.log(np.expm1(m))).astype(np.float32)
         return np.broadcast_to(zh[None, None, :], shape).copy()
-    noise = normals(w.seed, off["gate"], w.tokens).reshape(shape)
+    noise = normals_f32(w.seed, off["gate"], w.tokens).astype(np.float64).reshape(shape)
     if w.gate == "normal":
         z = w.lo + w.sigma * noise
     elif w.gate == "head_uniform":
@@ -168,7 +203,7 @@ def draw(w: Workload, with_dO: Optional[bool] = None):
     out = {}
     names = ["q", "k", "v"] + (["dO"] if with_dO else [])
     for name in names:
-        x = normals(w.seed, off[name], n).astype(np.float32)
+        x = normals_f32(w.seed, off[name], n)
         out[name] = (f32_to_bf16_bits(x) if w.dtype == "bf16" else x).reshape(shape)
     out["z"] = gate_logits(w)
     return out

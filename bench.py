@@ -221,6 +221,17 @@ def draw_inputs(w: wl.Workload, rank: int, cut: int = 0):
     return arrays
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """Largest `value` over all ranks (the timing rule: the slowest rank sets the job's time)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_fox(args, rank: int, world: int, local_rank: int):
     import torch
 
@@ -285,10 +296,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
     elapsed_ms = starts[0].elapsed_time(stops[-1])
     assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
-    if dist:
-        t = torch.tensor([elapsed_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
     flops_step = w.fwd_flops() + w.bwd_flops()
     value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
 
@@ -356,11 +364,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         e2e_step()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
     e2e_value = world * flops_step * args.steps / e2e_s / 1e12
 
     cpu = None

@@ -5,9 +5,12 @@
 //   P_ij = exp(x_ij - LSE_i)        (recomputed from the saved LSE)
 //   dP_ij = dO_i . v_j,  Delta_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - Delta_i)
 //   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
-//   gate: C_j = sum_i dS_ij (column sums; the row sums R_i = sum_j dS_ij are 0,
-//   since sum_j P_ij dP_ij = dO_i . O_i), then d a_t = -sum_{s>=t} C_s under
-//   the j+1 convention (-sum_{s>t} C_s under j), and dz_t = d a_t * sigmoid(-z_t).
+//   gate: R_i = sum_j dS_ij and C_j = sum_i dS_ij (row and column sums), then
+//   d a_t = sum_{s>=t} (R_s - C_s) under the j+1 convention (+ C_t under j), and
+//   dz_t = d a_t * sigmoid(-z_t). R_i is 0 in exact arithmetic, but Delta_i is
+//   formed from the bf16-rounded O, so the computed dS has small row sums;
+//   including them makes d a_t the sum of the computed dS over the entries that
+//   contain a_t, instead of accumulating those row errors along the sequence.
 //
 // Kernels, in launch order (the gate scan of the forward runs first):
 //   bwd_rows      Delta_i, the row offset rho_i = LSE_i log2 e - l_i, zeroes the dQ accumulator
@@ -15,7 +18,10 @@
 //                 S^T = K Q^T and dP^T = V dO^T (tcgen05, TMEM), P^T and dS^T in registers,
 //                 dV += P^T dO, dK += dS^T Q (A from TMEM), dQ_I = dS K (A from smem)
 //                 reduced into the fp32 accumulator, and the column sums C_j kept in
-//                 registers (the CTA owns every column j of its tile, no atomics).
+//                 registers (the CTA owns every column j of its tile, no atomics). The
+//                 dQ MMA of the last 64 output columns is widened by 16 columns whose
+//                 B operand is a column of ones, so it also yields this tile's part of
+//                 the row sums R_i (one atomic add per row and key tile).
 //   bwd_dq        dQ = scale * accumulator -> bf16
 //   bwd_gate      reverse prefix scan of C and the sigmoid chain rule -> dz
 #include <cuda_bf16.h>
@@ -36,7 +42,8 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int Npad, const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                                                       const float* __restrict__ rowloc, float* __restrict__ delta,
-                                                      float* __restrict__ rho, float* __restrict__ dqacc) {
+                                                      float* __restrict__ rho, float* __restrict__ rowsum,
+                                                      float* __restrict__ dqacc) {
   constexpr int E = D / 32;  // elements per lane
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -73,6 +80,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 #pragma unroll
   for (int e = 0; e < E; ++e) dq[e] = 0.f;
   if (lane == 0) {
+    rowsum[bh * Npad + i] = 0.f;
     delta[bh * Npad + i] = i < N ? acc : 0.f;
     rho[bh * Npad + i] =
         i < N ? lse[((size_t)b * N + i) * H + h] * kLog2e - rowloc[bh * Npad + i] : __int_as_float(0x7f800000);
@@ -88,6 +96,7 @@ struct BwdKParams {
   const float* delta;
   const float* rho;
   float* colsum;
+  float* rowsum;
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -105,7 +114,8 @@ struct BwdLayoutSmem {
   static constexpr int kRec = kDS + 32768;    // column record of tile J (528 B)
   static constexpr int kDR = kRec + 1024;     // Delta_I (512 B) then rho_I (512 B)
   static constexpr int kCs = kDR + 1024;      // column-sum exchange, 128 floats
-  static constexpr int kBars = kCs + 512;
+  static constexpr int kOnes = kCs + 1024;    // 1024-aligned: 128 rows x 64 bf16, column 0 = 1, rest 0 (MN-major B)
+  static constexpr int kBars = kOnes + 16384;
   static constexpr int kNumBars = 12;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -163,12 +173,16 @@ __device__ __forceinline__ void pds_chunk(uint32_t tA, uint32_t tB, int q0, int 
       if (kDiag && q0 + c < jr) x = -INFINITY;
       pv[e] = ex2_approx(x);
       dv[e] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
-      csum += dv[e];
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
     dd[2 * e4] = pack_bf16x2(dv[0], dv[1]);
     dd[2 * e4 + 1] = pack_bf16x2(dv[2], dv[3]);
+    // Column sums of the bf16-rounded dS, the same values the row sums R_i are
+    // formed from on the tensor core, so sum_s (R_s - C_s) over a suffix is the
+    // sum of one matrix's entries and carries no rounding drift along the sequence.
+    csum += (__uint_as_float(dd[2 * e4] << 16) + __uint_as_float(dd[2 * e4] & 0xffff0000u)) +
+            (__uint_as_float(dd[2 * e4 + 1] << 16) + __uint_as_float(dd[2 * e4 + 1] & 0xffff0000u));
   }
   // packed column of query pair (2c, 2c+1) is c = q / 2
   tmem_st16(tA + (q0 >> 1), pp);
@@ -220,6 +234,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  {
+    // Ones column for the row sums: element (row r, column c) of this 64-wide MN-major
+    // chunk sits in 16-byte piece (c / 8) ^ (r % 8) of row r; column 0 is 1.0, the rest 0.
+    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + L::kOnes);
+    for (int e = threadIdx.x; e < 16384 / 4; e += blockDim.x) {
+      const int r = e >> 5, word = e & 31;  // 32 words of 4 bytes per 128-byte row
+      ones[e] = (word == ((r & 7) << 2)) ? 0x3F80u : 0u;  // bf16 1.0 in the low half = column 0
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -273,9 +297,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
       constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
+      constexpr uint32_t idQR = idesc_bf16(128, 80, true, true);
       const uint32_t tA = tbase, tB = tbase + 128, tdK = tbase + 256, tdV = tbase + 256 + D;
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
-      const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS);
+      const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS), sOnes = smem_u32(sm + L::kOnes);
       bool ok = mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
       for (int u = 0; u < nI && ok; ++u) {
         const int st = u & 1;
@@ -306,14 +331,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
           umma_ts(tdK, tB + ks * 8, sdesc_sw128(sQs + ks * 2048, 16384, 1024), idKV, (u > 0 || ks > 0) ? 1u : 0u);
-        // dQ_I = dS K_J, 64 output columns per MMA (A = dS^T smem read as MN-major dS)
+        // dQ_I = dS K_J, 64 output columns per MMA (A = dS^T smem read as MN-major dS). The last
+        // one is 80 wide: its B operand continues past the K chunk into the ones chunk, so
+        // output column 64 is R_i's part from this key tile (columns 65..79 are zeros).
 #pragma unroll
         for (int x = 0; x < D / 64; ++x) {
+          const bool last = x == D / 64 - 1;
           const uint32_t tdq = (D == 128 && x == 0) ? tB + 64 : tA + 64;
+          const uint32_t kchunk = sK + x * 16384;
+          const uint32_t lbo = last ? sOnes - kchunk : 16384;
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_ss(tdq, sdesc_sw128(sdS + ks * 2048, 16384, 1024), sdesc_sw128(sK + x * 16384 + ks * 2048, 16384, 1024),
-                    idQ, ks > 0);
+            umma_ss(tdq, sdesc_sw128(sdS + ks * 2048, 16384, 1024), sdesc_sw128(kchunk + ks * 2048, lbo, 1024),
+                    last ? idQR : idQ, ks > 0);
         }
         umma_commit(&bars[BB_DQ]);
         umma_commit(&bars[BB_QEMPTY + st]);
@@ -403,6 +433,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             red_add_v4(dst + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                        __uint_as_float(r[e + 3]));
         }
+        if (ch == 1) {  // this key tile's part of R_i, in the column after the last dQ column
+          uint32_t rv;
+          tmem_ld1(tA + 128, rv);
+          tmem_ld_wait();
+          atomicAdd(p.rowsum + (size_t)bh * p.Npad + (size_t)I * kTile + jr, __uint_as_float(rv));
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars[BB_DQFREE]);
@@ -483,22 +519,24 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Np
 
 // ---------------------------------------------------------- gate backward
 // One CTA (1024 threads) per (b, h): reverse inclusive scan of the column
-// sums in chunks of 1024, from the end of the sequence.
+// sums minus the column sums in chunks of 1024, from the end of the sequence.
 __global__ void __launch_bounds__(1024) bwd_gate_kernel(int N, int H, int Npad, int bias_from_j,
-                                                       const float* __restrict__ colsum, const float* __restrict__ z,
+                                                       const float* __restrict__ colsum,
+                                                       const float* __restrict__ rowsum, const float* __restrict__ z,
                                                        float* __restrict__ dz) {
   __shared__ float wsum[32];
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh % H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* C = colsum + (size_t)bh * Npad;
+  const float* R = rowsum + (size_t)bh * Npad;
   float carry = 0.f;
   const int nchunks = (N + 1023) / 1024;
   for (int ck = nchunks - 1; ck >= 0; --ck) {
     // element t = ck*1024 + 1023 - tid, so the scan in tid order is a suffix scan in t
     const int t = ck * 1024 + 1023 - tid;
     const float c = t < N ? C[t] : 0.f;
-    float x = c;
+    float x = t < N ? R[t] - c : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -516,9 +554,9 @@ __global__ void __launch_bounds__(1024) bwd_gate_kernel(int N, int H, int Npad, 
       wsum[lane] = w;
     }
     __syncthreads();
-    const float incl = x + (warp > 0 ? wsum[warp - 1] : 0.f) + carry;  // sum_{s >= t} C_s
+    const float incl = x + (warp > 0 ? wsum[warp - 1] : 0.f) + carry;  // sum_{s >= t} (R_s - C_s)
     if (t < N) {
-      const float da = -(bias_from_j ? incl - c : incl);
+      const float da = bias_from_j ? incl + c : incl;
       const float zt = z[((size_t)b * N + t) * H + h];
       const float sig_neg = 1.f / (1.f + expf(zt));  // sigmoid(-z); 0 at z = +inf
       dz[((size_t)b * N + t) * H + h] = da * sig_neg;
@@ -538,6 +576,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   float* delta = reinterpret_cast<float*>(a.ws + w.delta);
   float* rho = reinterpret_cast<float*>(a.ws + w.rho);
   float* colsum = reinterpret_cast<float*>(a.ws + w.colsum);
+  float* rowsum = reinterpret_cast<float*>(a.ws + w.rowsum);
   float* dqacc = reinterpret_cast<float*>(a.ws + w.dqacc);
   uint32_t* err = reinterpret_cast<uint32_t*>(a.ws);
   const long long rows = (long long)a.B * g.Npad * a.H;
@@ -545,7 +584,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
     TraceScope trace("bwd_rows", s);
     bwd_rows_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
         a.B, a.N, a.H, g.Npad, static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        rowloc, delta, rho, dqacc);
+        rowloc, delta, rho, rowsum, dqacc);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -563,6 +602,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   p.delta = delta;
   p.rho = rho;
   p.colsum = colsum;
+  p.rowsum = rowsum;
   p.dqacc = dqacc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -585,7 +625,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   if (e != cudaSuccess) return e;
   {
     TraceScope trace("bwd_gate", s);
-    bwd_gate_kernel<<<g.BH, 1024, 0, s>>>(a.N, a.H, g.Npad, a.bias_from_j, colsum, a.z, a.dz);
+    bwd_gate_kernel<<<g.BH, 1024, 0, s>>>(a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz);
   }
   return cudaGetLastError();
 }

@@ -30,6 +30,7 @@ struct BwdLayout {
   size_t delta = 0;   // float [BH][Npad]   Delta_i = dO_i . O_i (0 past the sequence end)
   size_t rho = 0;     // float [BH][Npad]   LSE_i * log2 e - l_i: row offset to recompute P (+inf past the end)
   size_t colsum = 0;  // float [BH][Npad]   C_j = sum_i dS_ij
+  size_t rowsum = 0;  // float [BH][Npad]   R_i = sum_j dS_ij (0 in exact arithmetic; accumulated across key tiles)
   size_t dqacc = 0;   // float [BH][Npad][d] dQ accumulator (fp32, unscaled)
   size_t end = 0;
 };
@@ -64,6 +65,8 @@ inline BwdLayout bwd_layout(const GateLayout& g, int d) {
   w.rho = off;
   off = align_up(off + row, 256);
   w.colsum = off;
+  off = align_up(off + row, 256);
+  w.rowsum = off;
   off = align_up(off + row, 256);
   w.dqacc = off;
   off = align_up(off + row * (size_t)d, 256);

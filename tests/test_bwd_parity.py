@@ -104,10 +104,12 @@ def test_train_workload_sampled_heads():
     check_heads(w, heads=[(0, 0), (0, 15), (3, 7), (5, 2), (7, 15)])
 
 
-def test_backward_is_deterministic_except_dq():
+def test_backward_determinism():
+    """dK and dV are written without atomics and repeat bit for bit; dQ and dz
+    take fp32 atomic reductions across key tiles and repeat within rounding."""
     w = wl.Workload("bdet", 2, 700, 2, 128, "bf16", seed=21, gate="head_uniform", lo=0.5, hi=4.0, backward=True)
     a, g1 = run_fwd_bwd(w)
     _, g2 = run_fwd_bwd(w, arrays=a)
-    for n in (1, 2, 3):  # dK, dV, dz are written without atomics
+    for n in (1, 2):
         np.testing.assert_array_equal(g1[n], g2[n])
-    assert rel(g1[0], g2[0]) < 1e-2
+    assert rel(g1[0], g2[0]) < 1e-3 and rel(g1[3], g2[3]) < 1e-3

@@ -36,9 +36,9 @@ WORKLOAD = wl.Workload(
     "long_bf16_B1H32N16384d128", 1, 16384, 32, 128, "bf16", 2, gate="head_linspace", lo=0.0, hi=8.0, sigma=0.5,
     backward=True,
 )
-# CPU sample of the same workload: heads (0, 0..3), each restricted to its first 4096 tokens
+# CPU sample of the same workload: all 32 heads of batch 0, each restricted to its first 4096 tokens
 # (a causal prefix is a complete problem of its own), forward + backward.
-CPU_SAMPLE_HEADS = 4
+CPU_SAMPLE_HEADS = 32
 CPU_SAMPLE_TOKENS = 4096
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -401,7 +401,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("fox", "reference"), default="fox")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")

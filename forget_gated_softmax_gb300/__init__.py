@@ -42,6 +42,8 @@ EXPORTS = (
     "fox_version",
     "fox_trace_begin",
     "fox_trace_end",
+    "fox_fwd_noalloc",
+    "fox_noalloc_scratch_bytes",
 )
 
 
@@ -96,6 +98,10 @@ def lib() -> ctypes.CDLL:
         L.fox_status_string.restype = ctypes.c_char_p
         L.fox_version.argtypes = []
         L.fox_version.restype = i
+        L.fox_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp]
+        L.fox_fwd_noalloc.restype = i
+        L.fox_noalloc_scratch_bytes.argtypes = []
+        L.fox_noalloc_scratch_bytes.restype = sz
         L.fox_trace_begin.argtypes = []
         L.fox_trace_begin.restype = i
         L.fox_trace_end.argtypes = [ctypes.POINTER(fox_trace_record), i]
@@ -232,6 +238,24 @@ def fox_bwd(
     if st != 0:
         raise FoxError(st, "fox_bwd")
     return dq, dk, dv, dz
+
+
+def fox_fwd_noalloc(q, k, v, z, *, scale: float = 0.0, bias_from_j: bool = False, o=None, lse=None, stream=None):
+    """Forward with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory; see fox_fwd_noalloc in
+    include/fox.h). Output tensors are allocated here only when not passed."""
+    torch = _torch()
+    B, N, H, d = q.shape
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, N, H), dtype=torch.float32, device=q.device)
+    st = lib().fox_fwd_noalloc(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(o), _ptr(lse),
+                               _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_fwd_noalloc")
+    return o, lse
 
 
 def fox_check_error(ws, stream=None) -> int:

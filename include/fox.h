@@ -98,6 +98,28 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
                    size_t workspace_bytes, void* stream);
 
 /*
+ * Forward without a caller-provided workspace, for callers that cannot
+ * allocate device memory where they run this code (a plugin in a host
+ * application that owns all device memory, a latency-bound loop that cannot
+ * take an allocation's implicit synchronisation). The pages have no
+ * counterpart: this is a library convenience, not part of the method.
+ * Same arguments and results as fox_fwd, minus the workspace: the scratch
+ * for the gate terms is a fixed array of fox_noalloc_scratch_bytes() (16 MiB)
+ * compiled into the library, which every GPU that loads the library holds
+ * until the process exits. Problems whose fox_fwd_workspace_bytes exceeds it
+ * return FOX_ERR_WORKSPACE without touching the GPU. Allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library call). The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. All calls
+ * share the one array and the last call's contents stay in it: each call
+ * rewrites it completely (the error word included), and calls whose work
+ * overlaps on the GPU race on it. fox_check_error does not apply to it.
+ */
+fox_status fox_fwd_noalloc(const fox_params* p, const void* q, const void* k, const void* v, const float* z,
+                           void* o, float* lse, void* stream);
+size_t fox_noalloc_scratch_bytes(void);
+
+/*
  * Synchronises `stream`, reads and clears the device error word of
  * `workspace` (the one passed to the last fox_fwd / fox_bwd on it).
  * Returns FOX_OK, FOX_ERR_TIMEOUT or FOX_ERR_DEVICE, or FOX_ERR_CUDA if the

@@ -203,7 +203,7 @@ def workload_config(n_gpus: int):
                     f"z = b_h + 0.5 N(0,1), b_h = linspace(0, 8, 32)",
         "B": w.B, "H": w.H, "N": w.N, "d": w.d,
         "flops_per_step": w.fwd_flops() + w.bwd_flops(),
-        "l2": "inputs larger than L2: q, k, v, dO are 134 MB each, 537 MB read per step",
+        "l2": f"inputs larger than L2: q, k, v, dO are {w.tokens * w.d * 2 / 1e6:.0f} MB each",
         "parallelism": f"{n_gpus} rank(s), each an independent batch of heads (no collective)",
     }
 
@@ -405,7 +405,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("fox", "reference"), default="fox")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
+    ap.add_argument("--shape", default=None,
+                    help="B,N,H,d of a smaller case of the same workload recipe (profiling runs; not a bench line)")
     args = ap.parse_args()
+    if args.shape:
+        import dataclasses
+
+        global WORKLOAD
+        B, N, H, d = (int(x) for x in args.shape.split(","))
+        WORKLOAD = dataclasses.replace(WORKLOAD, name=f"long_recipe_B{B}H{H}N{N}d{d}", B=B, N=N, H=H, d=d)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

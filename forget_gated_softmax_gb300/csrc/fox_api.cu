@@ -32,12 +32,12 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d) {
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -209,8 +209,10 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
   CUtensorMap maps[4];
-  if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d) ||
-      !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[3], dO, p->B, p->N, p->H, p->d))
+  if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d, 64) ||
+      !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d, kTile) ||
+      !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d, kTile) ||
+      !make_bnhd_map(&maps[3], dO, p->B, p->N, p->H, p->d, 64))
     return FOX_ERR_CUDA;
   AttnBwdArgs a;
   a.B = p->B;

@@ -33,8 +33,6 @@
 namespace fox {
 namespace {
 
-constexpr int kBwdThreads = 320;
-constexpr int kRecBytes = kColRec * 4;  // 528
 
 // ------------------------------------------------------------------ rows
 // One warp per (b, i, h) with i in [0, Npad).
@@ -88,6 +86,18 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 }
 
 // ------------------------------------------------------------------ main
+// One CTA per (b, h, 128-key tile J). The query tiles I >= J are processed as
+// half-tiles g = 0, 1, ... of 64 queries (tile I = J + g/2, half g%2), software
+// pipelined over two tensor-memory buffers:
+//   MMA warp      S^T_g = K Q_g^T, dP^T_g = V dO_g^T into buffer g%2, then, once the
+//                 elementwise warps are done with g-1: dV += P^T_{g-1} dO_{g-1},
+//                 dK += dS^T_{g-1} Q_{g-1}, dQ^T_{g-1} = K^T dS^T_{g-1} (over the freed
+//                 buffer) and R_{g-1} = dS_{g-1} 1 (row sums, 16 spare columns).
+//   8 elementwise P^T, dS^T of g (thread = key row x 32 queries) while the tensor
+//     warps        core runs g-1 / g+1; column sums C_j in registers.
+//   4 readout     dQ^T_g reduced into the fp32 accumulator (thread = output column),
+//     warps       R_g added to the row sums, buffer g%2 handed back.
+//   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 struct BwdKParams {
   int B, N, H, nT, Npad;
   float scale2;  // scale * log2 e
@@ -103,20 +113,26 @@ struct BwdKParams {
   uint32_t* err;
 };
 
+constexpr int kHalf = 64;        // queries per half-tile
+constexpr int kStages = 3;       // Q / dO / Delta / rho stages
+constexpr int kBwdThreads = 448; // 14 warps
+
 template <int D>
 struct BwdLayoutSmem {
-  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kTileBytes = kTile * D * 2;  // K or V tile (128 keys)
+  static constexpr int kHalfBytes = kHalf * D * 2;  // Q or dO half-tile (64 queries)
   static constexpr int kK = 0;
   static constexpr int kV = kTileBytes;
-  static constexpr int kQ = 2 * kTileBytes;   // 2 stages
-  static constexpr int kDO = 4 * kTileBytes;  // 1 stage
-  static constexpr int kDS = 5 * kTileBytes;  // dS^T, 128 keys x 128 queries bf16 (32 KB)
-  static constexpr int kRec = kDS + 32768;    // column record of tile J (528 B)
-  static constexpr int kDR = kRec + 1024;     // Delta_I (512 B) then rho_I (512 B)
-  static constexpr int kCs = kDR + 1024;      // column-sum exchange, 128 floats
-  static constexpr int kOnes = kCs + 1024;    // 1024-aligned: 128 rows x 64 bf16, column 0 = 1, rest 0 (MN-major B)
-  static constexpr int kBars = kOnes + 16384;
-  static constexpr int kNumBars = 12;
+  static constexpr int kQ = 2 * kTileBytes;                    // kStages stages
+  static constexpr int kDO = kQ + kStages * kHalfBytes;        // kStages stages
+  static constexpr int kDS = kDO + kStages * kHalfBytes;       // 2 buffers of dS^T: 128 keys x 64 queries bf16
+  static constexpr int kZeros = kDS + 2 * 16384;               // 64-wide zero chunk (padding operand)
+  static constexpr int kOnes = kZeros + 16384;                 // K-major 16 x 128: row 0 ones, rest zeros (4 KB)
+  static constexpr int kDR = kOnes + 4096;                     // kStages x (Delta 256 B, rho 256 B)
+  static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
+  static constexpr int kCs = kRec + 1024;                      // column-sum exchange, 128 floats
+  static constexpr int kBars = kCs + 512;
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
@@ -124,45 +140,53 @@ struct BwdLayoutSmem {
 
 enum BwdBar {
   BB_KV = 0,
-  BB_QFULL = 1,   // +stage
-  BB_QEMPTY = 3,  // +stage
-  BB_DOFULL = 5,
-  BB_DOEMPTY = 6,
-  BB_SDP = 7,     // S^T and dP^T in TMEM
-  BB_PDS = 8,     // P^T, dS^T written (count 256)
-  BB_DQ = 9,      // dQ pair result in TMEM
-  BB_DQFREE = 10, // dQ read out (count 256)
-  BB_FINAL = 11,  // last dK/dV MMAs retired
+  BB_FULL = 1,    // +stage (3): Q, dO, Delta, rho of a half-tile landed
+  BB_EMPTY = 4,   // +stage (3): the MMAs reading that stage retired
+  BB_SDP = 7,     // +buffer (2): S^T, dP^T in tensor memory
+  BB_PDS = 9,     // +buffer (2): P^T, dS^T written (count 256)
+  BB_DQ = 11,     // +buffer (2): dQ^T and R in tensor memory; dS^T smem buffer free again
+  BB_DQFREE = 13, // +buffer (2): dQ^T read out, buffer free (count 128)
+  BB_FINAL = 15,  // last dK / dV MMAs retired
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-__device__ __forceinline__ void named_bar_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Barrier over `n` threads that also ORs a predicate across them: every thread gets the
+// same answer, so a group can agree to stop without anyone left waiting.
+__device__ __forceinline__ bool named_bar_any(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %3, 0;\n\t"
+      "barrier.red.or.pred po, %1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+__device__ __forceinline__ void red_add(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
 }
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// P^T and dS^T for 32 queries (columns q0 .. q0+31 of this thread's key row).
-// Writes packed bf16 pairs into 16 TMEM columns of each region and the dS^T
-// row piece into the swizzled shared-memory tile; accumulates the column sum.
+// P^T and dS^T for 32 queries of this thread's key row (columns c0 .. c0+31 of
+// the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
+// and [64+c0, 64+c0+32); packed bf16 P^T / dS^T go to [c0/2, c0/2+16) and
+// [64+c0/2, ...); the dS^T row piece goes to the swizzled smem buffer (queries
+// contiguous, MN-major). Accumulates the column sum of the bf16-rounded dS.
 template <bool kDiag>
-__device__ __forceinline__ void pds_chunk(uint32_t tA, uint32_t tB, int q0, int jr, float scale2, float cj,
-                                          const float* dlt, const float* rh, uint32_t sds_row, float& csum) {
-  uint32_t rs[32], rp[32];
-  tmem_ld32(tA + q0, rs);
-  tmem_ld32(tB + q0, rp);
-  tmem_ld_wait();
+__device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
+                                      const float* rh, uint32_t sds_row, float& csum, const uint32_t* rs,
+                                      const uint32_t* rp) {
   uint32_t pp[16], dd[16];
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
-    const float4 r4 = lds_f4(rh + q0 + 4 * e4);
-    const float4 d4 = lds_f4(dlt + q0 + 4 * e4);
+    const float4 r4 = lds_f4(rh + c0 + 4 * e4);
+    const float4 d4 = lds_f4(dlt + c0 + 4 * e4);
     const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
     const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
     float pv[4], dv[4];
@@ -170,7 +194,7 @@ __device__ __forceinline__ void pds_chunk(uint32_t tA, uint32_t tB, int q0, int 
     for (int e = 0; e < 4; ++e) {
       const int c = 4 * e4 + e;
       float x = fmaf(__uint_as_float(rs[c]), scale2, cj) - rr[e];
-      if (kDiag && q0 + c < jr) x = -INFINITY;
+      if (kDiag && qoff + c0 + c < jr) x = -INFINITY;  // query before key: masked
       pv[e] = ex2_approx(x);
       dv[e] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
     }
@@ -178,21 +202,17 @@ __device__ __forceinline__ void pds_chunk(uint32_t tA, uint32_t tB, int q0, int 
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
     dd[2 * e4] = pack_bf16x2(dv[0], dv[1]);
     dd[2 * e4 + 1] = pack_bf16x2(dv[2], dv[3]);
-    // Column sums of the bf16-rounded dS, the same values the row sums R_i are
-    // formed from on the tensor core, so sum_s (R_s - C_s) over a suffix is the
-    // sum of one matrix's entries and carries no rounding drift along the sequence.
+    // Column sums of the bf16-rounded dS: the same values the row sums R_i are formed
+    // from on the tensor core, so sum_s (R_s - C_s) over a suffix sums one matrix.
     csum += (__uint_as_float(dd[2 * e4] << 16) + __uint_as_float(dd[2 * e4] & 0xffff0000u)) +
             (__uint_as_float(dd[2 * e4 + 1] << 16) + __uint_as_float(dd[2 * e4 + 1] & 0xffff0000u));
   }
-  // packed column of query pair (2c, 2c+1) is c = q / 2
-  tmem_st16(tA + (q0 >> 1), pp);
-  tmem_st16(tB + (q0 >> 1), dd);
-  // dS^T row jr: queries q0 .. q0+31 are 16-byte pieces (q0 % 64) / 8 .. +3 of chunk q0 / 64
-  const uint32_t row = sds_row + (uint32_t)(q0 >> 6) * 16384u;
+  tmem_st16(tX + (c0 >> 1), pp);
+  tmem_st16(tX + 64 + (c0 >> 1), dd);
 #pragma unroll
   for (int pc = 0; pc < 4; ++pc) {
-    const int piece = ((q0 & 63) >> 3) + pc;
-    sts_v4(row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
+    const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
+    sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
   }
 }
 
@@ -213,35 +233,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int J = static_cast<int>(blockIdx.x) / BH;  // key tile; J = 0 has the most query tiles
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.H, h = bh % p.H;
-  const int nI = p.nT - J;
+  const int G = 2 * (p.nT - J);  // half-tiles
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[BB_KV], 1);
-    mbar_init(&bars[BB_QFULL + 0], 1);
-    mbar_init(&bars[BB_QFULL + 1], 1);
-    mbar_init(&bars[BB_QEMPTY + 0], 1);
-    mbar_init(&bars[BB_QEMPTY + 1], 1);
-    mbar_init(&bars[BB_DOFULL], 1);
-    mbar_init(&bars[BB_DOEMPTY], 1);
-    mbar_init(&bars[BB_SDP], 1);
-    mbar_init(&bars[BB_PDS], 256);
-    mbar_init(&bars[BB_DQ], 1);
-    mbar_init(&bars[BB_DQFREE], 256);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[BB_FULL + s], 1);
+      mbar_init(&bars[BB_EMPTY + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[BB_SDP + x], 1);
+      mbar_init(&bars[BB_PDS + x], 256);
+      mbar_init(&bars[BB_DQ + x], 1);
+      mbar_init(&bars[BB_DQFREE + x], 128);
+    }
     mbar_init(&bars[BB_FINAL], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   {
-    // Ones column for the row sums: element (row r, column c) of this 64-wide MN-major
-    // chunk sits in 16-byte piece (c / 8) ^ (r % 8) of row r; column 0 is 1.0, the rest 0.
-    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + L::kOnes);
-    for (int e = threadIdx.x; e < 16384 / 4; e += blockDim.x) {
-      const int r = e >> 5, word = e & 31;  // 32 words of 4 bytes per 128-byte row
-      ones[e] = (word == ((r & 7) << 2)) ? 0x3F80u : 0u;  // bf16 1.0 in the low half = column 0
+    // Constant operands. zeros: a 64-wide chunk of zeros (the upper M half of a padded
+    // A operand). ones: K-major 16 x 128 (two 64-key chunks of 16 rows x 128 B),
+    // row 0 all ones, so dS times it puts the row sums of dS in output column 0.
+    uint32_t* zw = reinterpret_cast<uint32_t*>(sm + L::kZeros);
+    for (int e = threadIdx.x; e < 16384 / 4; e += blockDim.x) zw[e] = 0u;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(sm + L::kOnes);
+    for (int e = threadIdx.x; e < 4096 / 4; e += blockDim.x) {
+      const int row = (e >> 5) & 15;  // 32 words per 128-byte row, 16 rows per 2 KB chunk
+      ow[e] = row == 0 ? 0x3F803F80u : 0u;
     }
     fence_proxy_async_smem();
   }
@@ -249,199 +272,199 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // TMEM columns: A = S^T / P^T [0,128), B = dP^T / dS^T [128,256), dK [256, 256+D), dV [256+D, 256+2D).
-  // dQ of a pair: D = 128 -> e in [0,64) at B+64, e in [64,128) at A+64;  D = 64 -> A+64.
+  // Tensor memory: buffer x at [128x, 128x+128): S^T [0,64) | dP^T [64,128) (P^T packed over
+  // [0,32), dS^T over [64,96); dQ^T later over [0,64), R over [64,80)); dK [256, 256+D), dV after it.
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
       tma_prefetch_desc(&tmap_do);
-      constexpr uint32_t tb = L::kTileBytes;
-      mbar_arrive_expect_tx(&bars[BB_KV], 2 * tb + kRecBytes);
+      constexpr uint32_t tb = L::kTileBytes, hb = L::kHalfBytes;
+      mbar_arrive_expect_tx(&bars[BB_KV], 2 * tb + kColRec * 4);
       for (int x = 0; x < D / 64; ++x) {
         tma_load_4d(sm + L::kK + x * 16384, &tmap_k, &bars[BB_KV], x * 64, h, J * kTile, b);
         tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
       }
-      bulk_load(sm + L::kRec, p.colrec + ((size_t)bh * p.nT + J) * kColRec, kRecBytes, &bars[BB_KV]);
-      int qfills[2] = {0, 0}, dofills = 0;
-      for (int u = 0; u < nI; ++u) {
-        const int I = J + u, st = u & 1;
-        if (u >= 2 && !mbar_wait(&bars[BB_QEMPTY + st], ((u >> 1) - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC))
+      bulk_load(sm + L::kRec, p.colrec + ((size_t)bh * p.nT + J) * kColRec, kColRec * 4, &bars[BB_KV]);
+      int fills[kStages] = {0, 0, 0};
+      for (int g = 0; g < G; ++g) {
+        const int st = g % kStages;
+        const int q0 = J * kTile + g * kHalf;
+        if (g >= kStages &&
+            !mbar_wait(&bars[BB_EMPTY + st], ((g / kStages) - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC))
           break;
-        mbar_arrive_expect_tx(&bars[BB_QFULL + st], tb);
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_4d(sm + L::kQ + st * tb + x * 16384, &tmap_q, &bars[BB_QFULL + st], x * 64, h, I * kTile, b);
-        ++qfills[st];
-        if (u >= 1 && !mbar_wait(&bars[BB_DOEMPTY], (u - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC)) break;
-        mbar_arrive_expect_tx(&bars[BB_DOFULL], tb + 1024);
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_4d(sm + L::kDO + x * 16384, &tmap_do, &bars[BB_DOFULL], x * 64, h, I * kTile, b);
-        const size_t roff = (size_t)bh * p.Npad + (size_t)I * kTile;
-        bulk_load(sm + L::kDR, p.delta + roff, 512, &bars[BB_DOFULL]);
-        bulk_load(sm + L::kDR + 512, p.rho + roff, 512, &bars[BB_DOFULL]);
-        ++dofills;
+        mbar_arrive_expect_tx(&bars[BB_FULL + st], 2 * hb + 512);
+        for (int x = 0; x < D / 64; ++x) {
+          tma_load_4d(sm + L::kQ + st * hb + x * 8192, &tmap_q, &bars[BB_FULL + st], x * 64, h, q0, b);
+          tma_load_4d(sm + L::kDO + st * hb + x * 8192, &tmap_do, &bars[BB_FULL + st], x * 64, h, q0, b);
+        }
+        const size_t roff = (size_t)bh * p.Npad + q0;
+        bulk_load(sm + L::kDR + st * 512, p.delta + roff, 256, &bars[BB_FULL + st]);
+        bulk_load(sm + L::kDR + st * 512 + 256, p.rho + roff, 256, &bars[BB_FULL + st]);
+        ++fills[st];
       }
       mbar_wait_drain(&bars[BB_KV], 0);
-      for (int st = 0; st < 2; ++st)
-        if (qfills[st] > 0) mbar_wait_drain(&bars[BB_QFULL + st], (qfills[st] - 1) & 1);
-      if (dofills > 0) mbar_wait_drain(&bars[BB_DOFULL], (dofills - 1) & 1);
+      for (int st = 0; st < kStages; ++st)
+        if (fills[st] > 0) mbar_wait_drain(&bars[BB_FULL + st], (fills[st] - 1) & 1);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t tb = L::kTileBytes;
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
-      constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
-      constexpr uint32_t idQR = idesc_bf16(128, 80, true, true);
-      const uint32_t tA = tbase, tB = tbase + 128, tdK = tbase + 256, tdV = tbase + 256 + D;
+      constexpr uint32_t hb = L::kHalfBytes;
+      constexpr uint32_t idSP = idesc_bf16(128, kHalf, false, false);  // S^T, dP^T: M keys, N queries
+      constexpr uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK: A from TMEM, B MN-major
+      constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
+      constexpr uint32_t idR = idesc_bf16(128, 16, true, false);       // R: A = dS (MN-major), B = ones (K-major)
+      const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
-      const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS), sOnes = smem_u32(sm + L::kOnes);
+      const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS);
+      const uint32_t sZeros = smem_u32(sm + L::kZeros), sOnes = smem_u32(sm + L::kOnes);
+      // A = K^T: M = d channels (MN-major 64-wide chunks 16 KB apart; D = 64 pads the upper half with zeros)
+      const uint32_t kt_lbo = D == 128 ? 16384u : sZeros - sK;
+
+      auto batch = [&](int g) -> bool {  // dV, dK, dQ^T, R of half-tile g (buffer g & 1)
+        const int x = g & 1, st = g % kStages;
+        const uint32_t tX = tbase + 128 * x;
+        const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb, sdSx = sdS + x * 16384;
+        if (!mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kHalf / 16; ++ks)  // dV += P^T dO (K = 64 queries)
+          umma_ts(tdV, tX + ks * 8, sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
+          umma_ts(tdK, tX + 64 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [0,64)
+          umma_ss(tX, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024), idQ,
+                  ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)  // R = dS 1 over [64,80) (A padded with the zero chunk)
+          umma_ss(tX + 64, sdesc_sw128(sdSx + ks * 2048, sZeros - sdSx, 1024),
+                  sdesc_sw128(sOnes + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), idR, ks > 0);
+        umma_commit(&bars[BB_DQ + x]);
+        umma_commit(&bars[BB_EMPTY + st]);
+        return true;
+      };
+
       bool ok = mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-      for (int u = 0; u < nI && ok; ++u) {
-        const int st = u & 1;
-        const uint32_t sQs = sQ + st * tb;
-        ok = mbar_wait(&bars[BB_QFULL + st], (u >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
-             mbar_wait(&bars[BB_DOFULL], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-        if (ok && u > 0) ok = mbar_wait(&bars[BB_DQFREE], (u - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+      for (int g = 0; g < G && ok; ++g) {
+        const int x = g & 1, st = g % kStages;
+        const uint32_t tX = tbase + 128 * x;
+        const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb;
+        ok = mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+        if (ok && g >= 2) ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          umma_ss(tA, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQs + off, 16, 1024), idS, ks > 0);
+          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;  // K / V tile: 128-row chunks
+          const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;   // Q / dO half-tile: 64-row chunks
+          umma_ss(tX, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQs + qoff, 16, 1024), idSP, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          umma_ss(tB, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024), idS, ks > 0);
+          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+          const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;
+          umma_ss(tX + 64, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(sdOs + qoff, 16, 1024), idSP, ks > 0);
         }
-        umma_commit(&bars[BB_SDP]);
-        ok = mbar_wait(&bars[BB_PDS], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (A from TMEM, B MN-major from smem)
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ts(tdV, tA + ks * 8, sdesc_sw128(sdO + ks * 2048, 16384, 1024), idKV, (u > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ts(tdK, tB + ks * 8, sdesc_sw128(sQs + ks * 2048, 16384, 1024), idKV, (u > 0 || ks > 0) ? 1u : 0u);
-        // dQ_I = dS K_J, 64 output columns per MMA (A = dS^T smem read as MN-major dS). The last
-        // one is 80 wide: its B operand continues past the K chunk into the ones chunk, so
-        // output column 64 is R_i's part from this key tile (columns 65..79 are zeros).
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x) {
-          const bool last = x == D / 64 - 1;
-          const uint32_t tdq = (D == 128 && x == 0) ? tB + 64 : tA + 64;
-          const uint32_t kchunk = sK + x * 16384;
-          const uint32_t lbo = last ? sOnes - kchunk : 16384;
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_ss(tdq, sdesc_sw128(sdS + ks * 2048, 16384, 1024), sdesc_sw128(kchunk + ks * 2048, lbo, 1024),
-                    last ? idQR : idQ, ks > 0);
-        }
-        umma_commit(&bars[BB_DQ]);
-        umma_commit(&bars[BB_QEMPTY + st]);
-        umma_commit(&bars[BB_DOEMPTY]);
+        umma_commit(&bars[BB_SDP + x]);
+        if (g >= 1) ok = batch(g - 1);
       }
+      if (ok && G > 0) batch(G - 1);
       umma_commit(&bars[BB_FINAL]);
       mbar_wait_drain(&bars[BB_FINAL], 0);
     }
     __syncwarp();
-  } else {
-    // ----------------------------------------------- P^T, dS^T, dQ, epilogue
-    const int wq = warp & 3, ch = warp >> 2;
-    const int jr = wq * 32 + lane;  // TMEM lane: key row for S^T/dP^T/dK/dV, query row for dQ
+  } else if (warp >= 8) {
+    // ------------------------------------------------ dQ^T and R readout
+    const int wq = warp & 3;
+    const int ln = wq * 32 + lane;  // TMEM lane: output channel e of dQ^T, query of R
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tA = tbase + lane_off, tB = tbase + 128 + lane_off;
-    const uint32_t tdK = tbase + 256 + lane_off, tdV = tbase + 256 + D + lane_off;
-    const uint32_t sds_row = smem_u32(sm + L::kDS) + (uint32_t)jr * 128u;
-    const float* dlt = reinterpret_cast<const float*>(sm + L::kDR);
-    const float* rh = dlt + kTile;
+    bool ok = true;
+    for (int g = 0; g < G && ok; ++g) {
+      const int x = g & 1;
+      const uint32_t tX = tbase + 128 * x + lane_off;
+      const int q0 = J * kTile + g * kHalf;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[32];
+#pragma unroll
+      for (int c = 0; c < kHalf; c += 32) {
+        tmem_ld32(tX + c, r);
+        tmem_ld_wait();
+        if (ln < D) {
+          float* dst = p.dqacc + ((size_t)bh * p.Npad + q0 + c) * D + ln;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red_add(dst + (size_t)i * D, __uint_as_float(r[i]));
+        }
+      }
+      if (wq < 2) {  // lanes 0..63: R of the half-tile's queries
+        uint32_t rv;
+        tmem_ld1(tX + 64, rv);
+        tmem_ld_wait();
+        atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[BB_DQFREE + x]);
+    }
+  } else {
+    // ------------------------------------------------------ P^T, dS^T, epilogue
+    const int wq = warp & 3, ch = warp >> 2;
+    const int jr = wq * 32 + lane;  // TMEM lane = key row of S^T, dP^T, dK, dV
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* rec = reinterpret_cast<const float*>(sm + L::kRec);
+    const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
     float csum = 0.f;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
-    float kap = 0.f, baseJ_hi = 0.f, baseJ_lo = 0.f;
-    if (ok) {
-      kap = rec[jr];
-      baseJ_hi = rec[kTile];
-      baseJ_lo = rec[kTile + 1];
-    }
-    const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
-    for (int u = 0; u < nI && ok; ++u) {
-      const int I = J + u;
+    ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
+    const float kap = ok ? rec[jr] : 0.f;
+    const float baseJ_hi = ok ? rec[kTile] : 0.f, baseJ_lo = ok ? rec[kTile + 1] : 0.f;
+    for (int g = 0; g < G && ok; ++g) {
+      const int x = g & 1, st = g % kStages;
+      const int I = J + (g >> 1), half = g & 1;
+      const uint32_t tX = tbase + 128 * x + lane_off;
+      const uint32_t sds_row = smem_u32(sm + L::kDS + x * 16384) + (uint32_t)jr * 128u;
+      const float* dlt = reinterpret_cast<const float*>(sm + L::kDR + st * 512);
+      const float* rh = dlt + kHalf;
       const float baseI_hi = recs[(size_t)I * kColRec + kTile], baseI_lo = recs[(size_t)I * kColRec + kTile + 1];
-      ok = mbar_wait(&bars[BB_SDP], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
-           mbar_wait(&bars[BB_DOFULL], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-      ok = __all_sync(0xffffffffu, ok);  // tcgen05 loads/stores below are warp-collective
+      ok = mbar_wait(&bars[BB_SDP + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
+           mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+      // dS^T smem buffer x is read by the dQ^T / R MMAs of half-tile g-2
+      if (ok && g >= 2) ok = mbar_wait(&bars[BB_DQ + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05 loads / stores below are warp-collective
       tc_fence_after();
       // x_ji (log2 units, minus the row offset) = scale2 * S^T_ji - kappa_j + (base_I - base_J) - rho_i
       const float cj = ((baseI_hi - baseJ_hi) + (baseI_lo - baseJ_lo)) - kap;
-      // Half ch = 1 overwrites packed columns that still hold half 0's S / dP values
-      // for queries 32..63: half 0 arrives on the quarter's barrier once it has read
-      // them. Half 0 arrives once per iteration it enters, even after a failed wait,
-      // so half 1 never waits on a barrier that cannot complete.
-      if (ch == 0) {
-        if (!ok) {
-          named_bar_arrive(1 + wq, 64);
-          break;
-        }
-        if (u == 0) {
-          pds_chunk<true>(tA, tB, 0, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-          pds_chunk<true>(tA, tB, 32, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-        } else {
-          pds_chunk<false>(tA, tB, 0, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-          pds_chunk<false>(tA, tB, 32, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-        }
-        named_bar_arrive(1 + wq, 64);
-      } else {
-        if (!ok) break;
-        named_bar_sync(1 + wq, 64);
-        if (u == 0) {
-          pds_chunk<true>(tA, tB, 64, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-          pds_chunk<true>(tA, tB, 96, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-        } else {
-          pds_chunk<false>(tA, tB, 64, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-          pds_chunk<false>(tA, tB, 96, jr, p.scale2, cj, dlt, rh, sds_row, csum);
-        }
+      const int c0 = ch * 32;
+      const int qoff = half * kHalf;  // query offset of this half inside tile I (for the diagonal mask)
+      // Half ch = 1 overwrites packed columns [16, 32) and [80, 96), which hold S^T / dP^T of
+      // queries 16..31 read by ch = 0. Both warps of the lane quarter load, then meet on the
+      // quarter's barrier every iteration (so neither can run an iteration ahead), and the
+      // barrier's OR tells both whether either of them has to stop.
+      uint32_t rs[32], rp[32];
+      if (ok) {
+        tmem_ld32(tX + c0, rs);
+        tmem_ld32(tX + 64 + c0, rp);
+        tmem_ld_wait();
       }
+      if (named_bar_any(1 + wq, 64, !ok)) {
+        ok = false;
+        break;
+      }
+      if (I == J)
+        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, csum, rs, rp);
+      else
+        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, csum, rs, rp);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[BB_PDS]);
-      // dQ of this pair: TMEM lane = query row of tile I
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_DQ], u & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        constexpr int kCols = D / 2;  // this half's output columns
-        const int e0 = ch * kCols;
-        const uint32_t src = (D == 128) ? (ch == 0 ? tB + 64 : tA + 64) : (tA + 64 + e0);
-        float* dst = p.dqacc + ((size_t)bh * p.Npad + (size_t)I * kTile + jr) * D + e0;
-#pragma unroll
-        for (int c = 0; c < kCols; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(src + c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                       __uint_as_float(r[e + 3]));
-        }
-        if (ch == 1) {  // this key tile's part of R_i, in the column after the last dQ column
-          uint32_t rv;
-          tmem_ld1(tA + 128, rv);
-          tmem_ld_wait();
-          atomicAdd(p.rowsum + (size_t)bh * p.Npad + (size_t)I * kTile + jr, __uint_as_float(rv));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[BB_DQFREE]);
+      mbar_arrive(&bars[BB_PDS + x]);
     }
     // Column sums: half 1 hands its partial to half 0 through shared memory.
     float* cs = reinterpret_cast<float*>(sm + L::kCs);
@@ -456,6 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       constexpr int kCols = D / 2;
       const int e0 = ch * kCols;
+      const uint32_t tdK = tbase + 256 + lane_off, tdV = tbase + 256 + D + lane_off;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t src = (which == 0 ? tdK : tdV) + e0;
@@ -485,7 +509,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }

@@ -126,10 +126,12 @@ struct AttnBwdArgs {
 // Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ
 // conversion and the reverse gate scan; the gate scan must already be in ws.
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w,
-                            const CUtensorMap* maps /* q, k, v, dO */, cudaStream_t s);
+                            const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box) */,
+                            cudaStream_t s);
 
-// Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 x 1 x 128 x 1 and 128-byte swizzle.
-// Returns false when the driver entry point is unavailable or encoding fails.
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d);
+// Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 channels x 1 head x
+// box_rows tokens x 1 batch and 128-byte swizzle. Returns false when the driver entry point is
+// unavailable or encoding fails.
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows = kTile);
 
 }  // namespace fox

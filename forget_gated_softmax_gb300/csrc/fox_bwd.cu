@@ -91,12 +91,13 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 // pipelined over two tensor-memory buffers:
 //   MMA warp      S^T_g = K Q_g^T, dP^T_g = V dO_g^T into buffer g%2, then, once the
 //                 elementwise warps are done with g-1: dV += P^T_{g-1} dO_{g-1},
-//                 dK += dS^T_{g-1} Q_{g-1}, dQ^T_{g-1} = K^T dS^T_{g-1} (over the freed
-//                 buffer) and R_{g-1} = dS_{g-1} 1 (row sums, 16 spare columns).
+//                 dK += dS^T_{g-1} Q_{g-1}, C_{g-1} = dS^T 1 (column sums), dQ^T_{g-1} =
+//                 K^T dS^T_{g-1} (over the freed buffer) and R_{g-1} = dS_{g-1} 1 (row sums).
 //   8 elementwise P^T, dS^T of g (thread = key row x 32 queries) while the tensor
-//     warps        core runs g-1 / g+1; column sums C_j in registers.
-//   4 readout     dQ^T_g reduced into the fp32 accumulator (thread = output column),
-//     warps       R_g added to the row sums, buffer g%2 handed back.
+//     warps        core runs g-1 / g+1.
+//   4 readout     copy dQ^T_g, R_g and C_g out of tensor memory (buffer g%2 is handed back
+//     warps       at once), then reduce dQ_g into the fp32 accumulator and R_g into the
+//                 row sums from registers; C stays in registers.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 struct BwdKParams {
   int B, N, H, nT, Npad;
@@ -130,8 +131,7 @@ struct BwdLayoutSmem {
   static constexpr int kOnes = kZeros + 16384;                 // K-major 16 x 128: row 0 ones, rest zeros (4 KB)
   static constexpr int kDR = kOnes + 4096;                     // kStages x (Delta 256 B, rho 256 B)
   static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
-  static constexpr int kCs = kRec + 1024;                      // column-sum exchange, 128 floats
-  static constexpr int kBars = kCs + 512;
+  static constexpr int kBars = kRec + 1024;
   static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -177,11 +177,12 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
 // the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
 // and [64+c0, 64+c0+32); packed bf16 P^T / dS^T go to [c0/2, c0/2+16) and
 // [64+c0/2, ...); the dS^T row piece goes to the swizzled smem buffer (queries
-// contiguous, MN-major). Accumulates the column sum of the bf16-rounded dS.
+// contiguous, MN-major). The row and column sums of dS are both formed on the
+// tensor core from these same bf16 values, so sum_s (R_s - C_s) over a suffix
+// sums one matrix and carries no rounding drift along the sequence.
 template <bool kDiag>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
-                                      const float* rh, uint32_t sds_row, float& csum, const uint32_t* rs,
-                                      const uint32_t* rp) {
+                                      const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp) {
   uint32_t pp[16], dd[16];
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
@@ -202,10 +203,6 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
     dd[2 * e4] = pack_bf16x2(dv[0], dv[1]);
     dd[2 * e4 + 1] = pack_bf16x2(dv[2], dv[3]);
-    // Column sums of the bf16-rounded dS: the same values the row sums R_i are formed
-    // from on the tensor core, so sum_s (R_s - C_s) over a suffix sums one matrix.
-    csum += (__uint_as_float(dd[2 * e4] << 16) + __uint_as_float(dd[2 * e4] & 0xffff0000u)) +
-            (__uint_as_float(dd[2 * e4 + 1] << 16) + __uint_as_float(dd[2 * e4 + 1] & 0xffff0000u));
   }
   tmem_st16(tX + (c0 >> 1), pp);
   tmem_st16(tX + 64 + (c0 >> 1), dd);
@@ -289,7 +286,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
       }
       bulk_load(sm + L::kRec, p.colrec + ((size_t)bh * p.nT + J) * kColRec, kColRec * 4, &bars[BB_KV]);
-      int fills[kStages] = {0, 0, 0};
+      int fills[kStages] = {};
       for (int g = 0; g < G; ++g) {
         const int st = g % kStages;
         const int q0 = J * kTile + g * kHalf;
@@ -319,6 +316,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK: A from TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
       constexpr uint32_t idR = idesc_bf16(128, 16, true, false);       // R: A = dS (MN-major), B = ones (K-major)
+      constexpr uint32_t idC = idesc_bf16(128, 16, false, false);      // C: A = dS^T (TMEM), B = ones (K-major)
       const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
       const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS);
@@ -338,6 +336,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
           umma_ts(tdK, tX + 64 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kHalf / 16; ++ks)  // C = dS^T 1 (column sums) over [96,112), before R overwrites [64,80)
+          umma_ts(tX + 96, tX + 64 + ks * 8, sdesc_sw128(sOnes + ks * 32, 16, 1024), idC, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [0,64)
           umma_ss(tX, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024), idQ,
@@ -381,10 +382,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 8) {
-    // ------------------------------------------------ dQ^T and R readout
+    // ---------------------------------------------- dQ^T, R and C readout
     const int wq = warp & 3;
-    const int ln = wq * 32 + lane;  // TMEM lane: output channel e of dQ^T, query of R
+    const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T, query of R, key of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float csum = 0.f;  // C_j for key j = ln, over all half-tiles
     bool ok = true;
     for (int g = 0; g < G && ok; ++g) {
       const int x = g & 1;
@@ -393,26 +395,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[32];
-#pragma unroll
-      for (int c = 0; c < kHalf; c += 32) {
-        tmem_ld32(tX + c, r);
-        tmem_ld_wait();
-        if (ln < D) {
-          float* dst = p.dqacc + ((size_t)bh * p.Npad + q0 + c) * D + ln;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) red_add(dst + (size_t)i * D, __uint_as_float(r[i]));
-        }
-      }
-      if (wq < 2) {  // lanes 0..63: R of the half-tile's queries
-        uint32_t rv;
-        tmem_ld1(tX + 64, rv);
-        tmem_ld_wait();
-        atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
-      }
+      uint32_t r0[32], r1[32], rv = 0, cv;
+      tmem_ld32(tX + 0, r0);
+      tmem_ld32(tX + 32, r1);
+      tmem_ld1(tX + 96, cv);
+      if (wq < 2) tmem_ld1(tX + 64, rv);  // lanes 0..63: R of the half-tile's queries
+      tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bars[BB_DQFREE + x]);
+      mbar_arrive(&bars[BB_DQFREE + x]);  // the buffer's contents are in registers now
+      csum += __uint_as_float(cv);
+      if (wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
+      if (ln < D) {  // dQ[q0 + i][e] += dQ^T[e][i]: each reduction covers 32 consecutive floats of a row
+        float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) red_add(dst + (size_t)i * D, __uint_as_float(r0[i]));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) red_add(dst + (size_t)(32 + i) * D, __uint_as_float(r1[i]));
+      }
     }
+    if (ok) p.colsum[(size_t)bh * p.Npad + J * kTile + ln] = csum;
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
     const int wq = warp & 3, ch = warp >> 2;
@@ -420,7 +421,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* rec = reinterpret_cast<const float*>(sm + L::kRec);
     const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
-    float csum = 0.f;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
     ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
@@ -458,20 +458,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       if (I == J)
-        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, csum, rs, rp);
+        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp);
       else
-        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, csum, rs, rp);
+        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BB_PDS + x]);
     }
-    // Column sums: half 1 hands its partial to half 0 through shared memory.
-    float* cs = reinterpret_cast<float*>(sm + L::kCs);
-    if (ch == 1) cs[jr] = csum;
-    named_bar_sync(5, 256);
     const int j = J * kTile + jr;
-    if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
     // dK, dV epilogue
     if (ok) ok = mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
     ok = __all_sync(0xffffffffu, ok);

@@ -112,6 +112,27 @@ __device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float sc
   return fmaxf(m0, m1);
 }
 
+// Upper bound of this row's t_j = scale2 * S_j - kappa_j over a tile without
+// masking: the column term is non-increasing along the tile (log f <= 0), so
+// max_j t_j <= scale2 * max_j S_j - kappa_127. Costs one FMNMX per element.
+__device__ __forceinline__ float row_bound(uint32_t tS, float scale2, float kappa_last) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int qt = 0; qt < 4; ++qt) {
+    uint32_t raw[32];
+    tmem_ld32(tS + 32 * qt, raw);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      m0 = fmaxf(m0, __uint_as_float(raw[j]));
+      m1 = fmaxf(m1, __uint_as_float(raw[j + 1]));
+      m2 = fmaxf(m2, __uint_as_float(raw[j + 2]));
+      m3 = fmaxf(m3, __uint_as_float(raw[j + 3]));
+    }
+  }
+  return fmaf(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)), scale2, -kappa_last);
+}
+
 // p_j = 2^(t_j - off) for the 128 columns, written back as bf16 pairs into
 // the first 64 columns of the same S row (chunk q's P lands on columns
 // [16q, 16q+16), which only hold S values already read). Returns sum_j p_j (fp32).
@@ -359,8 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float* kap = reinterpret_cast<const float*>(sm + L::kKappa + st * kKappaBytes);
         const float beta = (baseI_hi - kap[kTile]) + (baseI_lo - kap[kTile + 1]);
-        const float m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
-        const bool grow = m_cand > m_used + kRescaleThreshold;
+        // Cheap bound first; the exact row maximum only when the bound says the running
+        // maximum might be exceeded by more than the threshold (rare: the diagonal tile,
+        // visited first, holds the largest bias).
+        const float bound = row_bound(tS, p.scale2, kap[kTile - 1]) + beta;
+        float m_cand = bound;
+        bool grow = false;
+        if (__any_sync(0xffffffffu, bound > m_used + kRescaleThreshold)) {
+          m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
+          grow = m_cand > m_used + kRescaleThreshold;
+        }
         if (__any_sync(0xffffffffu, grow)) {
           // Some row's maximum grew by more than 2^8: rescale O and l of those rows
           // (alpha = 1 for the others; the TMEM loads/stores are warp-collective, so

@@ -91,13 +91,14 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 // pipelined over two tensor-memory buffers:
 //   MMA warp      S^T_g = K Q_g^T, dP^T_g = V dO_g^T into buffer g%2, then, once the
 //                 elementwise warps are done with g-1: dV += P^T_{g-1} dO_{g-1},
-//                 dK += dS^T_{g-1} Q_{g-1}, C_{g-1} = dS^T 1 (column sums), dQ^T_{g-1} =
-//                 K^T dS^T_{g-1} (over the freed buffer) and R_{g-1} = dS_{g-1} 1 (row sums).
+//                 dK += dS^T_{g-1} Q_{g-1}, C_{g-1} = dS^T 1 (column sums) and
+//                 dQ^T_{g-1} = K^T dS^T_{g-1} (over the freed buffer).
 //   8 elementwise P^T, dS^T of g (thread = key row x 32 queries) while the tensor
-//     warps        core runs g-1 / g+1.
-//   4 readout     copy dQ^T_g, R_g and C_g out of tensor memory (buffer g%2 is handed back
-//     warps       at once), then reduce dQ_g into the fp32 accumulator and R_g into the
-//                 row sums from registers; C stays in registers.
+//     warps        core runs g-1 / g+1; row sums R of g by a shuffle reduce-scatter
+//                  across the warp's 32 keys, added up in shared memory.
+//   4 readout     copy dQ^T_g and C_g out of tensor memory (buffer g%2 is handed back at
+//     warps       once), then reduce dQ_g into the fp32 accumulator and R_g into the
+//                 row sums; C stays in registers.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 struct BwdKParams {
   int B, N, H, nT, Npad;
@@ -131,7 +132,8 @@ struct BwdLayoutSmem {
   static constexpr int kOnes = kZeros + 16384;                 // K-major 16 x 128: row 0 ones, rest zeros (4 KB)
   static constexpr int kDR = kOnes + 4096;                     // kStages x (Delta 256 B, rho 256 B)
   static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
-  static constexpr int kBars = kRec + 1024;
+  static constexpr int kRsum = kRec + 1024;                    // [3 slots][4 lane quarters][64] row-sum partials
+  static constexpr int kBars = kRsum + 3 * 4 * kHalf * 4;
   static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -149,9 +151,6 @@ enum BwdBar {
   BB_FINAL = 15,  // last dK / dV MMAs retired
 };
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 // Barrier over `n` threads that also ORs a predicate across them: every thread gets the
 // same answer, so a group can agree to stop without anyone left waiting.
 __device__ __forceinline__ bool named_bar_any(int id, int n, bool pred) {
@@ -182,7 +181,8 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
 // sums one matrix and carries no rounding drift along the sequence.
 template <bool kDiag>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
-                                      const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp) {
+                                      const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp,
+                                      float* rsum) {
   uint32_t pp[16], dd[16];
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
@@ -211,6 +211,26 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
     sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
   }
+  // Row sums over this warp's 32 keys, of the same bf16 values: reduce-scatter across the
+  // lanes (five halving rounds), after which lane l holds query c0 + l's sum.
+  const int lane = jr & 31;
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    v[2 * k] = __uint_as_float(dd[k] << 16);
+    v[2 * k + 1] = __uint_as_float(dd[k] & 0xffff0000u);
+  }
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? v[k] : v[k + half];
+      const float keep = upper ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  rsum[c0 + lane] = v[0];  // this lane quarter's partial; the readout adds the four quarters
 }
 
 template <int D>
@@ -315,7 +335,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idSP = idesc_bf16(128, kHalf, false, false);  // S^T, dP^T: M keys, N queries
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK: A from TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
-      constexpr uint32_t idR = idesc_bf16(128, 16, true, false);       // R: A = dS (MN-major), B = ones (K-major)
       constexpr uint32_t idC = idesc_bf16(128, 16, false, false);      // C: A = dS^T (TMEM), B = ones (K-major)
       const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
@@ -337,16 +356,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
           umma_ts(tdK, tX + 64 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-        for (int ks = 0; ks < kHalf / 16; ++ks)  // C = dS^T 1 (column sums) over [96,112), before R overwrites [64,80)
+        for (int ks = 0; ks < kHalf / 16; ++ks)  // C = dS^T 1 (column sums) over [96,112)
           umma_ts(tX + 96, tX + 64 + ks * 8, sdesc_sw128(sOnes + ks * 32, 16, 1024), idC, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [0,64)
           umma_ss(tX, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024), idQ,
                   ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)  // R = dS 1 over [64,80) (A padded with the zero chunk)
-          umma_ss(tX + 64, sdesc_sw128(sdSx + ks * 2048, sZeros - sdSx, 1024),
-                  sdesc_sw128(sOnes + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), idR, ks > 0);
         umma_commit(&bars[BB_DQ + x]);
         umma_commit(&bars[BB_EMPTY + st]);
         return true;
@@ -392,15 +407,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const int q0 = J * kTile + g * kHalf;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA));
+      ok = mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
+           mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);  // row-sum partials
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t r0[32], r1[32], rv = 0, cv;
       tmem_ld32(tX + 0, r0);
       tmem_ld32(tX + 32, r1);
       tmem_ld1(tX + 96, cv);
-      if (wq < 2) tmem_ld1(tX + 64, rv);  // lanes 0..63: R of the half-tile's queries
       tmem_ld_wait();
+      if (wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
+        const float* rs = reinterpret_cast<const float*>(sm + L::kRsum) + (g % 3) * 4 * kHalf + ln;
+        rv = __float_as_uint((rs[0] + rs[kHalf]) + (rs[2 * kHalf] + rs[3 * kHalf]));
+      }
       tc_fence_before();
       mbar_arrive(&bars[BB_DQFREE + x]);  // the buffer's contents are in registers now
       csum += __uint_as_float(cv);
@@ -432,6 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t sds_row = smem_u32(sm + L::kDS + x * 16384) + (uint32_t)jr * 128u;
       const float* dlt = reinterpret_cast<const float*>(sm + L::kDR + st * 512);
       const float* rh = dlt + kHalf;
+      float* rsum = reinterpret_cast<float*>(sm + L::kRsum) + ((g % 3) * 4 + wq) * kHalf;
       const float baseI_hi = recs[(size_t)I * kColRec + kTile], baseI_lo = recs[(size_t)I * kColRec + kTile + 1];
       ok = mbar_wait(&bars[BB_SDP + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
            mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
@@ -458,9 +479,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       if (I == J)
-        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp);
+        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum);
       else
-        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp);
+        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();

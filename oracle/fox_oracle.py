@@ -11,6 +11,8 @@ Sources (web pages, cited by title and section):
                 ForgettingAttention: module docstring formula and forward().
   [foxwindow]   foxwindow README, sections "The window is a first-passage time"
                 and "ALiBi is the zero-variance limit".
+  [foxwindow-len] foxwindow README, "The window is a first-passage time"
+                (the epsilon-effective window) and "An exact two-moment law".
   [fast-tf]     fast-transformers "Creating a custom attention layer",
                 section "New Attention" (inputs already projected and split
                 into heads; einsum layout "nlhe,nshe->nhls", i.e. [B, N, H, d]).
@@ -36,6 +38,8 @@ fixed choice here):
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 __all__ = [
@@ -49,6 +53,7 @@ __all__ = [
     "backward",
     "gate_grad_bruteforce",
     "default_scale",
+    "effective_window",
 ]
 
 
@@ -232,3 +237,31 @@ def backward(q, k, v, z, dO, scale=None, bias_from_j=False):
                 q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], dO[b, :, h], scale, bias_from_j
             )
     return dQ, dK, dV, dz
+
+
+def effective_window(z, eps: float) -> np.ndarray:
+    """Epsilon-effective window of every query row of one head, z [N] -> int64 [N].
+
+    [foxwindow-len]: with the positive increments X_t = -log g_t (g = sigmoid(z)),
+    row i's window is the first-passage index of the walk read back from i,
+        N_i(eps) = inf{ n >= 1 : X_i + X_{i-1} + ... + X_{i-n+1} > L },  L = ln(1/eps),
+    i.e. one more than the largest distance n whose decay prod_{t=i-n+1..i} g_t is
+    still >= eps (the page names the latter "the largest distance with D >= eps" and
+    the former the first-passage index; this returns the first-passage index). The walk
+    has i+1 increments; if their sum never exceeds L the window is not reached inside
+    the sequence and the entry is -1.
+    Evaluated literally: accumulate the increments from i backwards until the sum
+    passes L. O(N * window); for tests.
+    """
+    X = -log_forget_gate(z)
+    L = math.log(1.0 / eps)
+    N = X.shape[0]
+    out = np.full(N, -1, dtype=np.int64)
+    for i in range(N):
+        acc = 0.0
+        for n in range(1, i + 2):
+            acc += X[i - n + 1]
+            if acc > L:
+                out[i] = n
+                break
+    return out

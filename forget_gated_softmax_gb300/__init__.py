@@ -44,6 +44,8 @@ EXPORTS = (
     "fox_trace_end",
     "fox_fwd_noalloc",
     "fox_noalloc_scratch_bytes",
+    "fox_window",
+    "fox_window_workspace_bytes",
 )
 
 
@@ -98,6 +100,10 @@ def lib() -> ctypes.CDLL:
         L.fox_status_string.restype = ctypes.c_char_p
         L.fox_version.argtypes = []
         L.fox_version.restype = i
+        L.fox_window_workspace_bytes.argtypes = [pp]
+        L.fox_window_workspace_bytes.restype = sz
+        L.fox_window.argtypes = [pp, vp, ctypes.c_double, vp, vp, sz, vp]
+        L.fox_window.restype = i
         L.fox_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp]
         L.fox_fwd_noalloc.restype = i
         L.fox_noalloc_scratch_bytes.argtypes = []
@@ -256,6 +262,28 @@ def fox_fwd_noalloc(q, k, v, z, *, scale: float = 0.0, bias_from_j: bool = False
     if st != 0:
         raise FoxError(st, "fox_fwd_noalloc")
     return o, lse
+
+
+def fox_window_workspace_bytes(params: fox_params) -> int:
+    return int(lib().fox_window_workspace_bytes(ctypes.byref(params)))
+
+
+def fox_window(z, eps: float, *, window=None, ws=None, stream=None):
+    """Epsilon-effective window per query row: z [B, N, H] fp32 -> int32 [B, N, H] (-1: not reached)."""
+    torch = _torch()
+    B, N, H = z.shape
+    params = make_params(B, N, H, 64)
+    if window is None:
+        window = torch.empty((B, N, H), dtype=torch.int32, device=z.device)
+    if ws is None:
+        ws = workspace(fox_window_workspace_bytes(params), z.device)
+    if not z.is_contiguous() or not window.is_contiguous():
+        raise ValueError("fox_window needs contiguous tensors")
+    st = lib().fox_window(ctypes.byref(params), _ptr(z), float(eps), _ptr(window), _ptr(ws), ws.numel(),
+                          _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_window")
+    return window
 
 
 def fox_check_error(ws, stream=None) -> int:

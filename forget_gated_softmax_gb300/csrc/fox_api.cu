@@ -236,6 +236,27 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   return launch_attn_bwd(a, g, w, maps, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
 }
 
+size_t fox_window_workspace_bytes(const fox_params* p) {
+  if (!p || p->B < 0 || p->N < 0 || p->H < 0) return 0;
+  if ((long long)p->B * p->H > kMaxTokens || (long long)p->B * p->H * (long long)p->N > kMaxTokens) return 0;
+  return window_workspace_bytes(p->B, p->N, p->H);
+}
+
+fox_status fox_window(const fox_params* p, const float* z, double eps, int32_t* window, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!p || p->B < 0 || p->N < 0 || p->H < 0) return FOX_ERR_INVALID_ARG;
+  if (!(eps > 0.0 && eps < 1.0)) return FOX_ERR_INVALID_ARG;
+  const size_t need = fox_window_workspace_bytes(p);
+  if (need == 0) return FOX_ERR_INVALID_ARG;
+  if (p->B == 0 || p->H == 0 || p->N == 0) return FOX_OK;
+  if (!z || !window || !aligned(z, 4) || !aligned(window, 4)) return FOX_ERR_INVALID_ARG;
+  fox_status st = check_workspace(workspace, workspace_bytes, need);
+  if (st != FOX_OK) return st;
+  return launch_window(z, p->B, p->N, p->H, eps, window, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FOX_OK
+             : FOX_ERR_CUDA;
+}
+
 fox_status fox_trace_begin(void) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
   g_trace_on = true;

@@ -129,6 +129,10 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const Bwd
                             const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box) */,
                             cudaStream_t s);
 
+// Epsilon-effective window per query row (fp64 prefix scan + binary search).
+cudaError_t launch_window(const float* z, int B, int N, int H, double eps, int* out, void* ws, cudaStream_t s);
+size_t window_workspace_bytes(int B, int N, int H);
+
 // Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 channels x 1 head x
 // box_rows tokens x 1 batch and 128-byte swizzle. Returns false when the driver entry point is
 // unavailable or encoding fails.

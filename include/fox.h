@@ -98,6 +98,20 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
                    size_t workspace_bytes, void* stream);
 
 /*
+ * Epsilon-effective window of every query row (foxwindow README, "The window is
+ * a first-passage time"): with X_t = -log sigmoid(z_t) and L = ln(1/eps),
+ *   window[b,i,h] = inf{ n >= 1 : X_i + X_{i-1} + ... + X_{i-n+1} > L },
+ * one more than the largest distance n whose decay prod_{t=i-n+1..i} f_t is
+ * still >= eps; -1 if the whole prefix (n = i+1) does not pass L. Uses the
+ * score form's sum from j+1 (bias_from_j, d, dtype and scale are ignored).
+ * z is [B,N,H] fp32, window [B,N,H] int32; 0 < eps < 1. The prefix sums and
+ * the comparisons are fp64. Workspace: fox_window_workspace_bytes(p).
+ */
+size_t fox_window_workspace_bytes(const fox_params* p);
+fox_status fox_window(const fox_params* p, const float* z, double eps, int32_t* window, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * Forward without a caller-provided workspace, for callers that cannot
  * allocate device memory where they run this code (a plugin in a host
  * application that owns all device memory, a latency-bound loop that cannot

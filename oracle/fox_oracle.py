@@ -95,12 +95,14 @@ def forget_bias(a: np.ndarray, bias_from_j: bool = False) -> np.ndarray:
     return c[:, None] - col[None, :]
 
 
-def attention_head(q, k, v, z, scale=None, bias_from_j=False, return_p=False):
+def attention_head(q, k, v, z, scale=None, bias_from_j=False, return_p=False, causal=True):
     """Forward of one (b, h): q, k, v [N, d], z [N] -> O [N, d], LSE [N].
 
     S_ij = scale * q_i . k_j + D_ij for j <= i, -inf for j > i
         [FoX-module, forward(): logits (q @ k^T) * scale + bias, causal
          triu(diagonal=1) mask set to -inf in decoder mode];
+    causal=False is the module's "encoder" mode: no mask, so the same outer
+    difference D_ij = c_i - c_j (positive for j > i) biases every key;
     LSE_i = M_i + ln sum_j exp(S_ij - M_i), M_i = max_j S_ij;
     P_ij = exp(S_ij - LSE_i) [FoX-module, forward(): softmax over keys];
     O_i = sum_j P_ij v_j [FoX-module, forward(): attn @ v].
@@ -116,7 +118,8 @@ def attention_head(q, k, v, z, scale=None, bias_from_j=False, return_p=False):
         return empty + (np.zeros((0, 0)),) if return_p else empty
     D = forget_bias(log_forget_gate(z), bias_from_j)
     S = scale * (q @ k.T) + D
-    S[np.triu(np.ones((N, N), dtype=bool), k=1)] = -np.inf
+    if causal:
+        S[np.triu(np.ones((N, N), dtype=bool), k=1)] = -np.inf
     M = S.max(axis=1)
     lse = M + np.log(np.exp(S - M[:, None]).sum(axis=1))
     P = np.exp(S - lse[:, None])
@@ -124,7 +127,7 @@ def attention_head(q, k, v, z, scale=None, bias_from_j=False, return_p=False):
     return (O, lse, P) if return_p else (O, lse)
 
 
-def attention_rows(q, k, v, z, rows, scale=None, bias_from_j=False):
+def attention_rows(q, k, v, z, rows, scale=None, bias_from_j=False, causal=True):
     """The forward of one (b, h) restricted to the query rows `rows`.
 
     Row i of O and LSE depends only on row i of S, so this is the same
@@ -144,14 +147,15 @@ def attention_rows(q, k, v, z, rows, scale=None, bias_from_j=False):
     O = np.empty((rows.size, v.shape[1]))
     lse = np.empty(rows.size)
     for n, i in enumerate(rows):
-        s = scale * (k[: i + 1] @ q[i]) + (c[i] - col[: i + 1])
+        last = i + 1 if causal else N
+        s = scale * (k[:last] @ q[i]) + (c[i] - col[:last])
         m = s.max()
         lse[n] = m + np.log(np.exp(s - m).sum())
-        O[n] = np.exp(s - lse[n]) @ v[: i + 1]
+        O[n] = np.exp(s - lse[n]) @ v[:last]
     return O, lse
 
 
-def forward(q, k, v, z, scale=None, bias_from_j=False):
+def forward(q, k, v, z, scale=None, bias_from_j=False, causal=True):
     """Batched forward. q, k, v [B, N, H, d]; z [B, N, H] -> O [B, N, H, d], LSE [B, N, H].
 
     Layout per [fast-tf, "New Attention"]: inputs already projected and split
@@ -164,12 +168,12 @@ def forward(q, k, v, z, scale=None, bias_from_j=False):
     for b in range(B):
         for h in range(H):
             O[b, :, h], lse[b, :, h] = attention_head(
-                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], scale, bias_from_j
+                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], scale, bias_from_j, causal=causal
             )
     return O, lse
 
 
-def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=False):
+def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=False, causal=True):
     """Gradients of one (b, h) by the chain rule through attention_head.
 
     dP_ij = dO_i . v_j;  Delta_i = dO_i . O_i;  dS_ij = P_ij (dP_ij - Delta_i)
@@ -178,7 +182,9 @@ def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=Fal
       j+1: d a_t = sum_{s>=t} (R_s - C_s)
       j  : d a_t = sum_{s>=t} (R_s - C_s) + C_t
     (a reverse prefix sum; gate_grad_bruteforce states the same quantity as
-    the double sum over the entries of D that contain a_t), and
+    the double sum over the entries of D that contain a_t). Without the causal
+    mask the same formula holds: D_ij = c_i - c_j contains +a_t when j < t <= i
+    and -a_t when i < t <= j, and both parts telescope into the suffix sums. And
     dz_t = d a_t * sigmoid(-z_t), since d/dz log sigmoid(z) = sigmoid(-z).
     """
     q = np.asarray(q, np.float64)
@@ -189,7 +195,7 @@ def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=Fal
     N, d = q.shape
     if scale is None:
         scale = default_scale(d)
-    O, lse, P = attention_head(q, k, v, z, scale, bias_from_j, return_p=True)
+    O, lse, P = attention_head(q, k, v, z, scale, bias_from_j, return_p=True, causal=causal)
     dP = dO @ v.T
     delta = (dO * O).sum(axis=1)
     dS = P * (dP - delta[:, None])
@@ -211,19 +217,23 @@ def backward_head(q, k, v, z, dO, scale=None, bias_from_j=False, return_sums=Fal
 def gate_grad_bruteforce(dS: np.ndarray, bias_from_j: bool = False) -> np.ndarray:
     """d a_t as the plain double sum over the bias entries that contain a_t.
 
-    j+1: a_t is in D_ij iff j < t <= i, so d a_t = sum_{i>=t} sum_{j<t} dS_ij.
-    j  : a_t is in D_ij iff j <= t <= i, so d a_t = sum_{i>=t} sum_{j<=t} dS_ij.
+    j+1: D_ij = c_i - c_j holds +a_t iff j < t <= i (and -a_t iff i < t <= j,
+         which only entries above the diagonal have), so
+         d a_t = sum_{i>=t} sum_{j<t} dS_ij - sum_{i<t} sum_{j>=t} dS_ij.
+    j  : D_ij = c_i - c_{j-1} holds +a_t iff j <= t <= i (and -a_t iff
+         i < t < j), so d a_t = sum_{i>=t} sum_{j<=t} dS_ij - sum_{i<t} sum_{j>t} dS_ij.
+    Under the causal mask dS is zero above the diagonal and the second sums vanish.
     O(N^3); for small N only.
     """
     N = dS.shape[0]
     da = np.zeros(N)
     for t in range(N):
-        jmax = t + 1 if bias_from_j else t
-        da[t] = dS[t:, :jmax].sum()
+        split = t + 1 if bias_from_j else t  # keys j < split take +a_t (for rows i >= t)
+        da[t] = dS[t:, :split].sum() - dS[:t, split:].sum()
     return da
 
 
-def backward(q, k, v, z, dO, scale=None, bias_from_j=False):
+def backward(q, k, v, z, dO, scale=None, bias_from_j=False, causal=True):
     """Batched backward over [B, N, H, d]: returns dQ, dK, dV [B, N, H, d], dz [B, N, H]."""
     q = np.asarray(q, np.float64)
     B, N, H, d = q.shape
@@ -234,12 +244,12 @@ def backward(q, k, v, z, dO, scale=None, bias_from_j=False):
     for b in range(B):
         for h in range(H):
             dQ[b, :, h], dK[b, :, h], dV[b, :, h], dz[b, :, h] = backward_head(
-                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], dO[b, :, h], scale, bias_from_j
+                q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], dO[b, :, h], scale, bias_from_j, causal=causal
             )
     return dQ, dK, dV, dz
 
 
-def effective_window(z, eps: float) -> np.ndarray:
+def effective_window(z, eps: float, rows=None) -> np.ndarray:
     """Epsilon-effective window of every query row of one head, z [N] -> int64 [N].
 
     [foxwindow-len]: with the positive increments X_t = -log g_t (g = sigmoid(z)),
@@ -251,17 +261,19 @@ def effective_window(z, eps: float) -> np.ndarray:
     has i+1 increments; if their sum never exceeds L the window is not reached inside
     the sequence and the entry is -1.
     Evaluated literally: accumulate the increments from i backwards until the sum
-    passes L. O(N * window); for tests.
+    passes L. O(N * window); for tests. With `rows`, only those rows are evaluated
+    (each row's window is defined on its own); the result then has len(rows) entries.
     """
     X = -log_forget_gate(z)
     L = math.log(1.0 / eps)
     N = X.shape[0]
-    out = np.full(N, -1, dtype=np.int64)
-    for i in range(N):
+    rows = range(N) if rows is None else [int(r) for r in rows]
+    out = np.full(len(rows), -1, dtype=np.int64)
+    for o, i in enumerate(rows):
         acc = 0.0
         for n in range(1, i + 2):
             acc += X[i - n + 1]
             if acc > L:
-                out[i] = n
+                out[o] = n
                 break
     return out

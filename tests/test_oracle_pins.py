@@ -330,3 +330,73 @@ def test_batched_backward_is_per_head():
             g = ora.backward_head(q[b, :, h], k[b, :, h], v[b, :, h], z[b, :, h], dO[b, :, h])
             for full, one in zip((dQ, dK, dV, dz), g):
                 np.testing.assert_array_equal(full[b, :, h], one)
+
+
+# ------------------------------------------------- non-causal ("encoder") mode
+
+
+def test_noncausal_open_gate_is_plain_softmax_attention():
+    N, d = 40, 8
+    q, k, v, _, _ = _rand_head(N, d, seed=61)
+    z = np.full(N, np.inf)
+    O, lse = ora.attention_head(q, k, v, z, causal=False)
+    tq, tk, tv = (torch.tensor(x)[None, None] for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=False)[0, 0].numpy()
+    np.testing.assert_allclose(O, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.tensor(d**-0.5 * q @ k.T), -1).numpy(), atol=1e-12)
+
+
+def test_noncausal_constant_gate_is_symmetric_alibi_with_sign():
+    """Encoder mode keeps the outer difference for every key: a constant gate gives
+    -m (i - j) everywhere, i.e. a bonus m (j - i) for keys after the query."""
+    N, d, m = 50, 8, 0.3
+    q, k, v, _, _ = _rand_head(N, d, seed=62)
+    z = np.full(N, -math.log(math.expm1(m)))
+    i, j = np.meshgrid(np.arange(N), np.arange(N), indexing="ij")
+    bias = torch.tensor(-m * (i - j).astype(np.float64))
+    O, lse = ora.attention_head(q, k, v, z, causal=False)
+    tq, tk, tv = (torch.tensor(x)[None, None] for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=bias[None, None])[0, 0].numpy()
+    np.testing.assert_allclose(O, ref, atol=1e-11)
+
+
+@pytest.mark.parametrize("from_j", [False, True])
+def test_noncausal_backward_matches_central_differences(from_j):
+    N, d = 9, 3
+    q, k, v, z, dO = _rand_head(N, d, gate_mu=0.5, gate_sigma=1.5, seed=63)
+    g = ora.backward_head(q, k, v, z, dO, bias_from_j=from_j, causal=False)
+
+    def loss(qq, kk, vv, zz):
+        O, _ = ora.attention_head(qq, kk, vv, zz, bias_from_j=from_j, causal=False)
+        return float((O * dO).sum())
+
+    h = 1e-6
+    for n, x in enumerate((q, k, v, z)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [q, k, v, z]
+            args_m = [q, k, v, z]
+            args_p[n], args_m[n] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.linalg.norm(num - g[n]) <= 1e-6 * np.linalg.norm(num) + 1e-8
+
+
+@pytest.mark.parametrize("from_j", [False, True])
+def test_noncausal_gate_grad_suffix_equals_signed_double_sum(from_j):
+    N, d = 30, 6
+    q, k, v, z, dO = _rand_head(N, d, seed=64)
+    _, _, _, _, ex = ora.backward_head(q, k, v, z, dO, bias_from_j=from_j, return_sums=True, causal=False)
+    np.testing.assert_allclose(ex["da"], ora.gate_grad_bruteforce(ex["dS"], from_j), atol=1e-12)
+
+
+def test_noncausal_rows_variant_matches_whole_head():
+    N, d = 140, 16
+    q, k, v, z, _ = _rand_head(N, d, seed=65)
+    O, lse = ora.attention_head(q, k, v, z, causal=False)
+    rows = [0, 70, 139]
+    Or, lr = ora.attention_rows(q, k, v, z, rows, causal=False)
+    np.testing.assert_allclose(Or, O[rows], atol=1e-12)
+    np.testing.assert_allclose(lr, lse[rows], atol=1e-12)

@@ -80,3 +80,11 @@ def test_renewal_laws_for_exponential_increments():
     se = math.sqrt(var_law / walks)
     assert abs(N.mean() - mean_law) < 5 * se
     assert abs(N.var() - var_law) < 0.05 * var_law
+
+
+def test_rows_subset_matches_full():
+    r = np.random.default_rng(5)
+    z = r.normal(1.0, 2.0, 500)
+    full = ora.effective_window(z, 1e-2)
+    rows = [0, 3, 250, 499]
+    np.testing.assert_array_equal(ora.effective_window(z, 1e-2, rows=rows), full[rows])

@@ -367,6 +367,27 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
     e2e_value = world * flops_step * args.steps / e2e_s / 1e12
 
+    # ---------------- rows SURVEY-style "next": timed separately, not part of the step
+    extra = {}
+    ws_w = fox.workspace(fox.fox_window_workspace_bytes(pf), "cuda")
+    win = torch.empty((w.B, w.N, w.H), dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        fox.fox_window(z, 1e-3, window=win, ws=ws_w, stream=stream)
+    torch.cuda.synchronize()
+    fox.trace_begin()
+    for _ in range(10):
+        fox.fox_window(z, 1e-3, window=win, ws=ws_w, stream=stream)
+    torch.cuda.synchronize()
+    wrec = fox.trace_end()
+    w_ms = sum(ms for _, ms in wrec) / 10
+    w_bytes = w.tokens * (4 + 8 + 8 + 4)  # z read, fp64 local sums written and read, int32 window written
+    extra["effective_window"] = {
+        "eps": 1e-3, "ms": w_ms, "launches_per_call": len(wrec) // 10,
+        "achieved": w_bytes / (w_ms * 1e-3) / 1e9, "unit": "GB/s", "bound": "hbm",
+        "frac": w_bytes / (w_ms * 1e-3) / 1e9 / measured_peaks()[0]["hbm_gbs"],
+        "rows_passing": int((win >= 0).sum().item()),
+    }
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, dt_cpu = oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
@@ -386,6 +407,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "clocks": clocks,
+            "next": extra,
             "breakdown": {
                 "step_ms_median": statistics.median(step_ms),
                 "fwd_attn_ms": fwd_ms, "fwd_attn_tflops": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,

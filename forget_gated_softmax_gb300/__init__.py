@@ -64,6 +64,7 @@ class fox_params(ctypes.Structure):
         ("dtype", ctypes.c_int),
         ("scale", ctypes.c_float),
         ("bias_from_j", ctypes.c_int),
+        ("non_causal", ctypes.c_int),
     ]
 
 
@@ -123,8 +124,9 @@ def fox_status_string(status: int) -> str:
         return STATUS_NAMES.get(int(status), f"status {status}")
 
 
-def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False) -> fox_params:
-    return fox_params(int(B), int(N), int(H), int(d), int(dtype), float(scale), int(bool(bias_from_j)))
+def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False, non_causal=False) -> fox_params:
+    return fox_params(int(B), int(N), int(H), int(d), int(dtype), float(scale), int(bool(bias_from_j)),
+                      int(bool(non_causal)))
 
 
 def fox_fwd_workspace_bytes(params: fox_params) -> int:
@@ -175,6 +177,7 @@ def fox_fwd(
     *,
     scale: float = 0.0,
     bias_from_j: bool = False,
+    non_causal: bool = False,
     o=None,
     lse=None,
     ws=None,
@@ -187,7 +190,7 @@ def fox_fwd(
     """
     torch = _torch()
     B, N, H, d = q.shape
-    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j)
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
@@ -217,6 +220,7 @@ def fox_bwd(
     *,
     scale: float = 0.0,
     bias_from_j: bool = False,
+    non_causal: bool = False,
     dq=None,
     dk=None,
     dv=None,
@@ -227,7 +231,7 @@ def fox_bwd(
     """Backward (bf16): returns (dQ, dK, dV, dz); dz is fp32 [B, N, H]."""
     torch = _torch()
     B, N, H, d = q.shape
-    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j)
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -101,6 +101,7 @@ fox_status check_params(const fox_params* p) {
   if (p->B < 0 || p->N < 0 || p->H < 0 || p->d <= 0) return FOX_ERR_INVALID_ARG;
   if (p->dtype != FOX_DTYPE_BF16 && p->dtype != FOX_DTYPE_F32) return FOX_ERR_INVALID_ARG;
   if (p->bias_from_j != 0 && p->bias_from_j != 1) return FOX_ERR_INVALID_ARG;
+  if (p->non_causal != 0 && p->non_causal != 1) return FOX_ERR_INVALID_ARG;
   if (!(p->scale >= 0.f) || std::isinf(p->scale)) return FOX_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return FOX_ERR_UNSUPPORTED;
   const long long BH = (long long)p->B * p->H;
@@ -179,7 +180,9 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
   a.rowloc = reinterpret_cast<const float*>(ws + g.rowloc);
   a.colrec = reinterpret_cast<const float*>(ws + g.colrec);
   a.err = reinterpret_cast<uint32_t*>(ws);
+  a.non_causal = p->non_causal;
   if (p->dtype == FOX_DTYPE_F32) {
+    if (p->non_causal) return FOX_ERR_UNSUPPORTED;
     if (p->B * p->H > 65535) return FOX_ERR_UNSUPPORTED;
     return launch_attn_fwd_f32(a, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
   }
@@ -220,6 +223,7 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   a.H = p->H;
   a.d = p->d;
   a.bias_from_j = p->bias_from_j;
+  a.non_causal = p->non_causal;
   a.scale = effective_scale(p);
   a.q = q;
   a.k = k;
@@ -233,6 +237,37 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   a.dv = dv;
   a.dz = dz;
   a.ws = static_cast<char*>(workspace);
+  if (p->non_causal) {
+    // Without the causal mask the gate gradient is a small difference of large
+    // row and column sums of dS = P (dP - Delta), and a Delta_i = dO_i . O_i
+    // taken from the bf16 O (or from an O built with bf16 P) moves it by
+    // several percent. Re-run the forward once in its Delta mode: P enters the
+    // P V product as two bf16 terms, and Delta comes from the fp32 accumulator;
+    // O and LSE are not written.
+    CUtensorMap fmaps[3];
+    if (!make_bnhd_map(&fmaps[0], q, p->B, p->N, p->H, p->d)) return FOX_ERR_CUDA;
+    fmaps[1] = maps[1];
+    fmaps[2] = maps[2];
+    AttnFwdArgs f;
+    f.B = p->B;
+    f.N = p->N;
+    f.H = p->H;
+    f.d = p->d;
+    f.scale = a.scale;
+    f.non_causal = 1;
+    f.q = q;
+    f.k = k;
+    f.v = v;
+    f.o = nullptr;
+    f.lse = nullptr;
+    f.rowloc = reinterpret_cast<const float*>(a.ws + g.rowloc);
+    f.colrec = reinterpret_cast<const float*>(a.ws + g.colrec);
+    f.err = reinterpret_cast<uint32_t*>(a.ws);
+    f.dO_for_delta = dO;
+    f.delta_out = reinterpret_cast<float*>(a.ws + w.delta);
+    if (launch_attn_fwd_bf16(f, fmaps, g.nT, g.Npad, s) != cudaSuccess) return FOX_ERR_CUDA;
+    a.delta_ready = 1;
+  }
   return launch_attn_bwd(a, g, w, maps, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
 }
 

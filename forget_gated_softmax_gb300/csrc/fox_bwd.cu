@@ -13,17 +13,17 @@
 //   contain a_t, instead of accumulating those row errors along the sequence.
 //
 // Kernels, in launch order (the gate scan of the forward runs first):
-//   bwd_rows      Delta_i, the row offset rho_i = LSE_i log2 e - l_i, zeroes the dQ accumulator
-//   bwd_main      one CTA per (b, h, 128-key tile J), looping over query tiles I >= J:
-//                 S^T = K Q^T and dP^T = V dO^T (tcgen05, TMEM), P^T and dS^T in registers,
-//                 dV += P^T dO, dK += dS^T Q (A from TMEM), dQ_I = dS K (A from smem)
-//                 reduced into the fp32 accumulator, and the column sums C_j kept in
-//                 registers (the CTA owns every column j of its tile, no atomics). The
-//                 dQ MMA of the last 64 output columns is widened by 16 columns whose
-//                 B operand is a column of ones, so it also yields this tile's part of
-//                 the row sums R_i (one atomic add per row and key tile).
+//   bwd_rows      Delta_i, the row offset rho_i = LSE_i log2 e - l_i; zeroes the dQ
+//                 accumulator and the row sums
+//   bwd_main      one CTA per (b, h, 128-key tile J) over the query tiles I >= J
+//                 (all I when not causal), pipelined over 64-query half-tiles:
+//                 S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q and
+//                 dQ^T = K^T dS^T on the tensor core (tcgen05, TMEM), dQ reduced into
+//                 an fp32 accumulator; the column sums C_j stay in registers (the CTA
+//                 owns every column j of its tile) and the row sums R_i are reduced
+//                 across lanes and added into a global accumulator once per half-tile.
 //   bwd_dq        dQ = scale * accumulator -> bf16
-//   bwd_gate      reverse prefix scan of C and the sigmoid chain rule -> dz
+//   bwd_gate      reverse prefix scan of (R - C) and the sigmoid chain rule -> dz
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
                                                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                                                       const float* __restrict__ rowloc, float* __restrict__ delta,
                                                       float* __restrict__ rho, float* __restrict__ rowsum,
-                                                      float* __restrict__ dqacc) {
+                                                      float* __restrict__ dqacc, int delta_ready) {
   constexpr int E = D / 32;  // elements per lane
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -79,29 +79,30 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
   for (int e = 0; e < E; ++e) dq[e] = 0.f;
   if (lane == 0) {
     rowsum[bh * Npad + i] = 0.f;
-    delta[bh * Npad + i] = i < N ? acc : 0.f;
+    if (!delta_ready || i >= N) delta[bh * Npad + i] = i < N ? acc : 0.f;
     rho[bh * Npad + i] =
         i < N ? lse[((size_t)b * N + i) * H + h] * kLog2e - rowloc[bh * Npad + i] : __int_as_float(0x7f800000);
   }
 }
 
 // ------------------------------------------------------------------ main
-// One CTA per (b, h, 128-key tile J). The query tiles I >= J are processed as
-// half-tiles g = 0, 1, ... of 64 queries (tile I = J + g/2, half g%2), software
+// One CTA per (b, h, 128-key tile J). The query tiles I >= J (every I when not
+// causal) are processed as half-tiles g = 0, 1, ... of 64 queries, software
 // pipelined over two tensor-memory buffers:
 //   MMA warp      S^T_g = K Q_g^T, dP^T_g = V dO_g^T into buffer g%2, then, once the
 //                 elementwise warps are done with g-1: dV += P^T_{g-1} dO_{g-1},
-//                 dK += dS^T_{g-1} Q_{g-1}, C_{g-1} = dS^T 1 (column sums) and
-//                 dQ^T_{g-1} = K^T dS^T_{g-1} (over the freed buffer).
+//                 dK += dS^T_{g-1} Q_{g-1} and dQ^T_{g-1} = K^T dS^T_{g-1} (over the
+//                 freed buffer).
 //   8 elementwise P^T, dS^T of g (thread = key row x 32 queries) while the tensor
-//     warps        core runs g-1 / g+1; row sums R of g by a shuffle reduce-scatter
-//                  across the warp's 32 keys, added up in shared memory.
-//   4 readout     copy dQ^T_g and C_g out of tensor memory (buffer g%2 is handed back at
-//     warps       once), then reduce dQ_g into the fp32 accumulator and R_g into the
-//                 row sums; C stays in registers.
+//     warps        core runs g-1 / g+1; fp32 column sums C in registers, row sums R of g
+//                  by a shuffle reduce-scatter across the warp's 32 keys.
+//   4 readout     copy dQ^T_g out of tensor memory (buffer g%2 is handed back at once),
+//     warps       then reduce it into the fp32 dQ accumulator and R_g (the four lane
+//                 quarters' partials) into the row sums.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 struct BwdKParams {
   int B, N, H, nT, Npad;
+  int non_causal;
   float scale2;  // scale * log2 e
   float scale;
   const float* colrec;
@@ -129,11 +130,11 @@ struct BwdLayoutSmem {
   static constexpr int kDO = kQ + kStages * kHalfBytes;        // kStages stages
   static constexpr int kDS = kDO + kStages * kHalfBytes;       // 2 buffers of dS^T: 128 keys x 64 queries bf16
   static constexpr int kZeros = kDS + 2 * 16384;               // 64-wide zero chunk (padding operand)
-  static constexpr int kOnes = kZeros + 16384;                 // K-major 16 x 128: row 0 ones, rest zeros (4 KB)
-  static constexpr int kDR = kOnes + 4096;                     // kStages x (Delta 256 B, rho 256 B)
+  static constexpr int kDR = kZeros + 16384;                    // kStages x (Delta 256 B, rho 256 B)
   static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
   static constexpr int kRsum = kRec + 1024;                    // [3 slots][4 lane quarters][64] row-sum partials
-  static constexpr int kBars = kRsum + 3 * 4 * kHalf * 4;
+  static constexpr int kCs = kRsum + 3 * 4 * kHalf * 4;        // column-sum exchange, 128 floats
+  static constexpr int kBars = kCs + 512;
   static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -182,27 +183,29 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
 template <bool kDiag>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
                                       const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp,
-                                      float* rsum) {
+                                      float* rsum, float& csum) {
   uint32_t pp[16], dd[16];
+  float v[32];  // fp32 dS of this row's 32 queries, for the row and column sums
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
     const float4 r4 = lds_f4(rh + c0 + 4 * e4);
     const float4 d4 = lds_f4(dlt + c0 + 4 * e4);
     const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
     const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-    float pv[4], dv[4];
+    float pv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = 4 * e4 + e;
       float x = fmaf(__uint_as_float(rs[c]), scale2, cj) - rr[e];
       if (kDiag && qoff + c0 + c < jr) x = -INFINITY;  // query before key: masked
       pv[e] = ex2_approx(x);
-      dv[e] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
+      v[c] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
+      csum += v[c];
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
-    dd[2 * e4] = pack_bf16x2(dv[0], dv[1]);
-    dd[2 * e4 + 1] = pack_bf16x2(dv[2], dv[3]);
+    dd[2 * e4] = pack_bf16x2(v[4 * e4], v[4 * e4 + 1]);
+    dd[2 * e4 + 1] = pack_bf16x2(v[4 * e4 + 2], v[4 * e4 + 3]);
   }
   tmem_st16(tX + (c0 >> 1), pp);
   tmem_st16(tX + 64 + (c0 >> 1), dd);
@@ -211,15 +214,9 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
     sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
   }
-  // Row sums over this warp's 32 keys, of the same bf16 values: reduce-scatter across the
-  // lanes (five halving rounds), after which lane l holds query c0 + l's sum.
+  // Row sums over this warp's 32 keys: reduce-scatter across the lanes (five halving
+  // rounds), after which lane l holds query c0 + l's sum.
   const int lane = jr & 31;
-  float v[32];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    v[2 * k] = __uint_as_float(dd[k] << 16);
-    v[2 * k + 1] = __uint_as_float(dd[k] & 0xffff0000u);
-  }
 #pragma unroll
   for (int half = 16; half >= 1; half >>= 1) {
     const bool upper = (lane & half) != 0;
@@ -250,7 +247,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int J = static_cast<int>(blockIdx.x) / BH;  // key tile; J = 0 has the most query tiles
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.H, h = bh % p.H;
-  const int G = 2 * (p.nT - J);  // half-tiles
+  // Half-tiles of 64 queries: causal, query tiles I = J .. nT-1; non-causal, all of them.
+  const bool causal = !p.non_causal;
+  const int I_first = causal ? J : 0;
+  const int G = 2 * (p.nT - I_first);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[BB_KV], 1);
@@ -273,16 +273,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_relinquish();
   }
   {
-    // Constant operands. zeros: a 64-wide chunk of zeros (the upper M half of a padded
-    // A operand). ones: K-major 16 x 128 (two 64-key chunks of 16 rows x 128 B),
-    // row 0 all ones, so dS times it puts the row sums of dS in output column 0.
+    // Constant operand: a 64-wide chunk of zeros, the upper M half of K^T when D = 64.
     uint32_t* zw = reinterpret_cast<uint32_t*>(sm + L::kZeros);
     for (int e = threadIdx.x; e < 16384 / 4; e += blockDim.x) zw[e] = 0u;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(sm + L::kOnes);
-    for (int e = threadIdx.x; e < 4096 / 4; e += blockDim.x) {
-      const int row = (e >> 5) & 15;  // 32 words per 128-byte row, 16 rows per 2 KB chunk
-      ow[e] = row == 0 ? 0x3F803F80u : 0u;
-    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -309,7 +302,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int fills[kStages] = {};
       for (int g = 0; g < G; ++g) {
         const int st = g % kStages;
-        const int q0 = J * kTile + g * kHalf;
+        const int q0 = I_first * kTile + g * kHalf;
         if (g >= kStages &&
             !mbar_wait(&bars[BB_EMPTY + st], ((g / kStages) - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC))
           break;
@@ -335,11 +328,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idSP = idesc_bf16(128, kHalf, false, false);  // S^T, dP^T: M keys, N queries
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK: A from TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
-      constexpr uint32_t idC = idesc_bf16(128, 16, false, false);      // C: A = dS^T (TMEM), B = ones (K-major)
       const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
       const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS);
-      const uint32_t sZeros = smem_u32(sm + L::kZeros), sOnes = smem_u32(sm + L::kOnes);
+      const uint32_t sZeros = smem_u32(sm + L::kZeros);
       // A = K^T: M = d channels (MN-major 64-wide chunks 16 KB apart; D = 64 pads the upper half with zeros)
       const uint32_t kt_lbo = D == 128 ? 16384u : sZeros - sK;
 
@@ -355,9 +347,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
           umma_ts(tdK, tX + 64 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kHalf / 16; ++ks)  // C = dS^T 1 (column sums) over [96,112)
-          umma_ts(tX + 96, tX + 64 + ks * 8, sdesc_sw128(sOnes + ks * 32, 16, 1024), idC, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [0,64)
           umma_ss(tX, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024), idQ,
@@ -401,21 +390,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int wq = warp & 3;
     const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T, query of R, key of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    float csum = 0.f;  // C_j for key j = ln, over all half-tiles
     bool ok = true;
     for (int g = 0; g < G && ok; ++g) {
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
-      const int q0 = J * kTile + g * kHalf;
+      const int q0 = I_first * kTile + g * kHalf;
       ok = mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
            mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);  // row-sum partials
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32], rv = 0, cv;
+      uint32_t r0[32], r1[32], rv = 0;
       tmem_ld32(tX + 0, r0);
       tmem_ld32(tX + 32, r1);
-      tmem_ld1(tX + 96, cv);
       tmem_ld_wait();
       if (wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
         const float* rs = reinterpret_cast<const float*>(sm + L::kRsum) + (g % 3) * 4 * kHalf + ln;
@@ -423,7 +410,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars[BB_DQFREE + x]);  // the buffer's contents are in registers now
-      csum += __uint_as_float(cv);
       if (wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
       if (ln < D) {  // dQ[q0 + i][e] += dQ^T[e][i]: each reduction covers 32 consecutive floats of a row
         float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
@@ -433,7 +419,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i = 0; i < 32; ++i) red_add(dst + (size_t)(32 + i) * D, __uint_as_float(r1[i]));
       }
     }
-    if (ok) p.colsum[(size_t)bh * p.Npad + J * kTile + ln] = csum;
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
     const int wq = warp & 3, ch = warp >> 2;
@@ -441,13 +426,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* rec = reinterpret_cast<const float*>(sm + L::kRec);
     const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
+    float csum = 0.f;  // C_j for key j = jr over this warp's queries of every half-tile
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
     ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
     const float baseJ_hi = ok ? rec[kTile] : 0.f, baseJ_lo = ok ? rec[kTile + 1] : 0.f;
     for (int g = 0; g < G && ok; ++g) {
       const int x = g & 1, st = g % kStages;
-      const int I = J + (g >> 1), half = g & 1;
+      const int I = I_first + (g >> 1), half = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const uint32_t sds_row = smem_u32(sm + L::kDS + x * 16384) + (uint32_t)jr * 128u;
       const float* dlt = reinterpret_cast<const float*>(sm + L::kDR + st * 512);
@@ -478,16 +464,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = false;
         break;
       }
-      if (I == J)
-        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum);
+      if (causal && I == J)
+        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
       else
-        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum);
+        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BB_PDS + x]);
     }
+    // Column sums: half ch = 1 hands its partial to ch = 0 through shared memory.
+    float* cs = reinterpret_cast<float*>(sm + L::kCs);
+    if (ch == 1) cs[jr] = csum;
+    named_bar_any(5, 256, false);
     const int j = J * kTile + jr;
+    if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
     // dK, dV epilogue
     if (ok) ok = mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
     ok = __all_sync(0xffffffffu, ok);
@@ -624,7 +615,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
     TraceScope trace("bwd_rows", s);
     bwd_rows_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
         a.B, a.N, a.H, g.Npad, static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        rowloc, delta, rho, rowsum, dqacc);
+        rowloc, delta, rho, rowsum, dqacc, a.delta_ready);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -636,6 +627,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   p.H = a.H;
   p.nT = g.nT;
   p.Npad = g.Npad;
+  p.non_causal = a.non_causal;
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.colrec = colrec;

@@ -29,6 +29,10 @@
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
 // P (bf16) overwrites the first 64 columns of its S buffer and feeds the P V
 // MMA straight from tensor memory.
+//
+// Delta mode (kDelta, for the non-causal backward): P is written as two bf16
+// terms over all 128 columns and both feed the P V product, so O is accurate
+// to fp32 rounding; the epilogue writes dO_i . O_i per row instead of O and LSE.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,12 +48,18 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum whi
 
 struct FwdKParams {
   int B, N, H, nT, nQB, Npad;
+  int non_causal;
   float scale2;  // scale * log2 e
   const float* rowloc;
   const float* colrec;
   __nv_bfloat16* o;
   float* lse;
   uint32_t* err;
+  // Delta mode (used by the non-causal backward): instead of O and LSE, write
+  // delta[bh][i] = dO_i . O_i with O_i from the fp32 accumulator of a P V
+  // product whose P is split into two bf16 terms.
+  const __nv_bfloat16* dO;
+  float* delta;
 };
 
 template <int D>
@@ -136,7 +146,10 @@ __device__ __forceinline__ float row_bound(uint32_t tS, float scale2, float kapp
 // p_j = 2^(t_j - off) for the 128 columns, written back as bf16 pairs into
 // the first 64 columns of the same S row (chunk q's P lands on columns
 // [16q, 16q+16), which only hold S values already read). Returns sum_j p_j (fp32).
-template <bool kDiag>
+// kSplit: p = hi + lo with hi = bf16(p), lo = bf16(p - hi) (about 16 significant
+// bits together); chunk q's hi goes to columns [32q, 32q+16) and lo to
+// [32q+16, 32q+32), the chunk's own columns, and both feed the P V product.
+template <bool kDiag, bool kSplit = false>
 __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float scale2, float off, int r) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -145,6 +158,7 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
     tmem_ld32(tS + 32 * qt, raw);
     tmem_ld_wait();
     uint32_t pk[16];
+    uint32_t lo[kSplit ? 16 : 1];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;
@@ -166,13 +180,25 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
       s1 += pr[1] + pr[3];
       pk[2 * j4] = pack_bf16x2(pr[0], pr[1]);
       pk[2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
+      if (kSplit) {
+        // The low halves of the packed pairs hold the even columns.
+        lo[2 * j4] = pack_bf16x2(pr[0] - __uint_as_float(pk[2 * j4] << 16),
+                                 pr[1] - __uint_as_float(pk[2 * j4] & 0xffff0000u));
+        lo[2 * j4 + 1] = pack_bf16x2(pr[2] - __uint_as_float(pk[2 * j4 + 1] << 16),
+                                     pr[3] - __uint_as_float(pk[2 * j4 + 1] & 0xffff0000u));
+      }
     }
-    tmem_st16(tS + 16 * qt, pk);
+    if (kSplit) {
+      tmem_st16(tS + 32 * qt, pk);
+      tmem_st16(tS + 32 * qt + 16, lo);
+    } else {
+      tmem_st16(tS + 16 * qt, pk);
+    }
   }
   return s0 + s1;
 }
 
-template <int D>
+template <int D, bool kDelta>
 __global__ void __launch_bounds__(kThreads, 1)
     fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const FwdKParams p) {
@@ -190,12 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H, h = bh % p.H;
   // Q tile k covers rows [128*I_k, 128*I_k + 128). KV tiles are streamed in
   // sequence order s = 0, 1, ..., nJ-1 with J = Jtop - s; tile k takes part
-  // for s >= first_k (its own diagonal tile is s = first_k).
+  // for s >= first_k. Causal: the stream starts at the last diagonal tile and
+  // tile k's first tile is its own diagonal. Non-causal: every tile, from the
+  // last one back (the bias c_i - c_j grows with j, so the largest bias comes first).
   const int I0 = 2 * qb, I1 = 2 * qb + 1;
   const bool has1 = I1 < p.nT;
-  const int Jtop = has1 ? I1 : I0;
+  const bool causal = !p.non_causal;
+  const int Jtop = causal ? (has1 ? I1 : I0) : p.nT - 1;
   const int nJ = Jtop + 1;
-  const int first0 = has1 ? 1 : 0;
+  const int first0 = (causal && has1) ? 1 : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q], 1);
@@ -283,9 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int k, int st, bool acc) {
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ts(tO[k], tS[k] + ks * 8, sdesc_sw128(sV + st * tb + ks * 2048, 16384, 1024), idO,
-                  (acc || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t dv = sdesc_sw128(sV + st * tb + ks * 2048, 16384, 1024);
+          if (kDelta) {  // P = hi + lo: chunk ks/2 holds hi at +0 and lo at +16 columns
+            const uint32_t a = tS[k] + 32 * (ks >> 1) + 8 * (ks & 1);
+            umma_ts(tO[k], a, dv, idO, (acc || ks > 0) ? 1u : 0u);
+            umma_ts(tO[k], a + 16, dv, idO, 1u);
+          } else {
+            umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
+          }
+        }
       };
       bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
                 mbar_wait(&bars[B_KFULL + 0], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
@@ -347,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;   // row within the Q tile
     const int I = k ? I1 : I0;
     const int first = k ? 0 : first0;
-    const int nJk = (k == 1 && !has1) ? 0 : I + 1;
+    const int nJk = (k == 1 && !has1) ? 0 : (causal ? I + 1 : p.nT);
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tbase + k * 128 + lane_off;
     const uint32_t tO = tbase + 256 + k * D + lane_off;
@@ -358,15 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float row_term = p.rowloc[(size_t)bh * p.Npad + i];
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true;
-      // Diagonal tile first (u = 0; base_I - base_J = 0 there).
+      // First tile (u = 0): exact row maximum, then one pass. Causal: the diagonal tile
+      // (base_I - base_J = 0), masked; non-causal: the last tile, unmasked.
       ok = mbar_wait(&bars[B_SFULL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
            mbar_wait(&bars[B_VFULL + (first & 1)], (first >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
       ok = __all_sync(0xffffffffu, ok);  // the tcgen05 loads below are warp-collective
       if (ok) {
         tc_fence_after();
         const float* kap = reinterpret_cast<const float*>(sm + L::kKappa + (first & 1) * kKappaBytes);
-        m_used = row_max<true>(tS, kap, p.scale2, r);
-        l_sum = exp_pass<true>(tS, kap, p.scale2, m_used, r);
+        // The first tile holds the largest bias (base_I - base_J is its offset; 0 on the diagonal).
+        const float beta0 = (baseI_hi - kap[kTile]) + (baseI_lo - kap[kTile + 1]);
+        if (causal) {
+          m_used = row_max<true>(tS, kap, p.scale2, r);
+          l_sum = exp_pass<true, kDelta>(tS, kap, p.scale2, m_used, r);
+        } else {
+          m_used = row_max<false>(tS, kap, p.scale2, r) + beta0;
+          l_sum = exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta0, r);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_PFULL + k]);
@@ -408,14 +452,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (grow) m_used = m_cand;
         }
-        l_sum += exp_pass<false>(tS, kap, p.scale2, m_used - beta, r);
+        l_sum += exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta, r);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_PFULL + k]);
       }
       if (ok) ok = mbar_wait(&bars[B_OFINAL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
       ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
+      if (kDelta && ok) {
+        tc_fence_after();
+        const float inv = 1.f / l_sum;
+        float dot = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait();
+          if (i < p.N) {
+            const uint4* g = reinterpret_cast<const uint4*>(p.dO + (((size_t)b * p.N + i) * p.H + h) * D + c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint4 w = g[q4];
+              const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                dot = fmaf(__uint_as_float(wv[e] << 16), __uint_as_float(o[8 * q4 + 2 * e]), dot);
+                dot = fmaf(__uint_as_float(wv[e] & 0xffff0000u), __uint_as_float(o[8 * q4 + 2 * e + 1]), dot);
+              }
+            }
+          }
+        }
+        if (i < p.N) p.delta[(size_t)bh * p.Npad + i] = dot * inv;
+      } else if (!kDelta && ok) {
         tc_fence_after();
         const float inv = 1.f / l_sum;
 #pragma unroll
@@ -453,7 +521,9 @@ template <int D>
 cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
   using L = FwdLayout<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fox_attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  const bool delta = a.delta_out != nullptr;
+  auto kernel = delta ? fox_attn_fwd_kernel<D, true> : fox_attn_fwd_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdKParams p;
   p.B = a.B;
@@ -461,6 +531,9 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   p.H = a.H;
   p.nT = nT;
   p.nQB = (nT + 1) / 2;
+  p.non_causal = a.non_causal;
+  p.dO = static_cast<const __nv_bfloat16*>(a.dO_for_delta);
+  p.delta = a.delta_out;
   p.Npad = Npad;
   p.scale2 = a.scale * kLog2e;
   p.rowloc = a.rowloc;
@@ -471,8 +544,8 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   const long long blocks = (long long)p.nQB * a.B * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
-    TraceScope trace("attn_fwd", s);
-    fox_attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], p);
+    TraceScope trace(delta ? "attn_fwd_delta" : "attn_fwd", s);
+    kernel<<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], p);
   }
   return cudaGetLastError();
 }

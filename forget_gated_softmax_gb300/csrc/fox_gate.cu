@@ -67,6 +67,12 @@ __global__ void __launch_bounds__(256) gate_tile_scan_kernel(const float* __rest
       float4 rl = make_float4(incl[0], incl[1], incl[2], incl[3]);
       *reinterpret_cast<float4*>(rowloc + bh * Npad + t0 + lane * 4) = rl;
       float4 cl = bias_from_j ? make_float4(incl[0] - a[0], incl[1] - a[1], incl[2] - a[2], incl[3] - a[3]) : rl;
+      // keys past the sequence end get an infinite column term: x = ... - kappa = -inf, p = 0
+      const int tl = t0 + lane * 4;
+      if (tl + 0 >= N) cl.x = INFINITY;
+      if (tl + 1 >= N) cl.y = INFINITY;
+      if (tl + 2 >= N) cl.z = INFINITY;
+      if (tl + 3 >= N) cl.w = INFINITY;
       *reinterpret_cast<float4*>(colrec + (bh * nT + T) * kColRec + lane * 4) = cl;
       if (lane == 31) tiletot[bh * nT + T] = incl[3];
     }

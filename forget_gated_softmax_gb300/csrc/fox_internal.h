@@ -16,7 +16,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Gate terms the attention kernels read, all in log2 units (natural value * log2 e).
 //   rowloc[bh][t]   l_t  = sum_{l = 128*T .. t} a_l          (T = t / 128; inclusive, tile-local)
 //   colrec[bh][T]   { kappa_j for j in tile T (tile-local column term:
-//                     inclusive for the j+1 convention, exclusive for the j convention),
+//                     inclusive for the j+1 convention, exclusive for the j convention;
+//                     +inf past the sequence end, which removes those keys from every row),
 //                     base_T hi, base_T lo, 0, 0 },  base_T = sum_{l < 128*T} a_l (fp64 scan, split hi+lo)
 //   tiletot[bh][T]  sum of a over tile T (fp32, scratch between the two gate kernels)
 // so that, for i in tile I and j in tile J, D_ij * log2 e = l_i - kappa_j + (base_I - base_J).
@@ -91,6 +92,7 @@ cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_
 
 struct AttnFwdArgs {
   int B, N, H, d;
+  int non_causal;
   float scale;
   const void* q;
   const void* k;
@@ -100,6 +102,10 @@ struct AttnFwdArgs {
   const float* rowloc;
   const float* colrec;
   uint32_t* err;
+  // When delta_out is set, the kernel writes delta_out[bh][i] = dO_i . O_i (O in fp32)
+  // instead of O and LSE (rows i < N; layout [BH][Npad]).
+  const void* dO_for_delta = nullptr;
+  float* delta_out = nullptr;
 };
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v */, int nT, int Npad,
@@ -108,6 +114,7 @@ cudaError_t launch_attn_fwd_f32(const AttnFwdArgs& a, int nT, int Npad, cudaStre
 
 struct AttnBwdArgs {
   int B, N, H, d, bias_from_j;
+  int non_causal;
   float scale;
   const void* q;
   const void* k;
@@ -121,6 +128,9 @@ struct AttnBwdArgs {
   void* dv;
   float* dz;
   char* ws;  // workspace base (gate layout, then the backward layout)
+  // Set when Delta of rows i < N is already in the backward layout (the forward
+  // kernel's Delta epilogue wrote it); the row kernel then only writes the padding.
+  int delta_ready = 0;
 };
 
 // Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ

@@ -6,7 +6,7 @@
  *   f_t = sigmoid(z_t),  a_t = log f_t,  c_t = sum_{l<=t} a_l
  *   D_ij = c_i - c_j          (bias_from_j = 0, the default; D_ii = 0)
  *   D_ij = c_i - c_{j-1}      (bias_from_j = 1; c_{-1} = 0)
- *   S_ij = scale * q_i . k_j + D_ij  for j <= i  (causal; j > i excluded)
+ *   S_ij = scale * q_i . k_j + D_ij  for j <= i  (causal; j > i excluded unless non_causal)
  *   LSE_i = ln sum_{j<=i} exp(S_ij),  O_i = sum_{j<=i} exp(S_ij - LSE_i) v_j
  * Sources: "Forgetting Transformer (FoX) Attention" module source
  * (frankenstein-transformer docs, fox_attn: module docstring formula and
@@ -69,6 +69,9 @@ typedef struct fox_params {
   int dtype;       /* FOX_DTYPE_BF16 (tensor cores) or FOX_DTYPE_F32 (forward only) */
   float scale;     /* multiplies q.k only; 0 selects d^-1/2 (module __init__: head_dim ** -0.5) */
   int bias_from_j; /* 0: D_ij = sum_{l=j+1}^{i} log f_l (module code, foxwindow); 1: sum_{l=j}^{i} (module docstring) */
+  int non_causal;  /* 0: causal (the module's "decoder" mode, the default); 1: every key, the module's
+                      "encoder" mode, where the same outer difference D_ij = c_i - c_j (positive for
+                      j > i) biases keys after the query too. bf16 forward and backward only. */
 } fox_params;
 
 /* Workspace bytes fox_fwd / fox_bwd need for these params (0 if params are invalid). */
@@ -91,7 +94,12 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
  * upstream gradient dO; writes dq, dk, dv [B,N,H,d] bf16 and dz [B,N,H] fp32.
  * Steps: gate scan, Delta_i = dO_i . O_i, the fused recompute-and-backward
  * attention kernel (dK, dV, dQ accumulator and the column sums of dS), the
- * dQ conversion and the reverse gate scan.
+ * dQ conversion and the reverse gate scan. With non_causal = 1, Delta is not
+ * taken from the bf16 O: the forward kernel runs once more in a mode whose
+ * P V product carries P as two bf16 terms and which writes dO_i . O_i from the
+ * fp32 accumulator (the gate gradient is a small difference of large sums of
+ * dS there, and the bf16 rounding of O moves it by percents). O still must
+ * be the forward's output; the extra pass costs about 1.5 forwards.
  */
 fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,
                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dz, void* workspace,

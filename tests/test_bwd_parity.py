@@ -25,16 +25,17 @@ def _gpu():
     fox.lib()
 
 
-def run_fwd_bwd(w: wl.Workload, scale=0.0, arrays=None):
+def run_fwd_bwd(w: wl.Workload, scale=0.0, arrays=None, non_causal=False):
     import forget_gated_softmax_gb300 as fox
 
     arrays = arrays if arrays is not None else wl.draw(w, with_dO=True)
     t = to_torch(arrays, "bf16")
-    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], scale=scale, bias_from_j=w.bias_from_j)
-    params = fox.make_params(w.B, w.N, w.H, w.d, 0, scale, w.bias_from_j)
+    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], scale=scale, bias_from_j=w.bias_from_j,
+                         non_causal=non_causal)
+    params = fox.make_params(w.B, w.N, w.H, w.d, 0, scale, w.bias_from_j, non_causal)
     ws = fox.workspace(fox.fox_bwd_workspace_bytes(params), "cuda")
     grads = fox.fox_bwd(t["q"], t["k"], t["v"], t["z"], o, lse, t["dO"], scale=scale, bias_from_j=w.bias_from_j,
-                        ws=ws)
+                        non_causal=non_causal, ws=ws)
     assert fox.fox_check_error(ws) == 0
     torch.cuda.synchronize()
     return arrays, [tensor_f64(g) for g in grads]
@@ -45,8 +46,8 @@ def rel(g, r):
     return np.linalg.norm(g - r) / n if n > 0 else np.linalg.norm(g)
 
 
-def check_heads(w: wl.Workload, heads=None, scale=0.0):
-    arrays, (dq, dk, dv, dz) = run_fwd_bwd(w, scale)
+def check_heads(w: wl.Workload, heads=None, scale=0.0, non_causal=False):
+    arrays, (dq, dk, dv, dz) = run_fwd_bwd(w, scale, non_causal=non_causal)
     for g in (dq, dk, dv, dz):
         assert np.isfinite(g).all()
     x = exact(arrays, "bf16")
@@ -55,7 +56,7 @@ def check_heads(w: wl.Workload, heads=None, scale=0.0):
     got = {n: [] for n in ref}
     for b, h in heads:
         r = ora.backward_head(x["q"][b, :, h], x["k"][b, :, h], x["v"][b, :, h], x["z"][b, :, h], x["dO"][b, :, h],
-                              scale=scale or None, bias_from_j=w.bias_from_j)
+                              scale=scale or None, bias_from_j=w.bias_from_j, causal=not non_causal)
         for n, rr, gg in zip(("dq", "dk", "dv", "dz"), r, (dq, dk, dv, dz)):
             ref[n].append(rr)
             got[n].append(gg[b, :, h])
@@ -113,3 +114,11 @@ def test_backward_determinism():
     for n in (1, 2):
         np.testing.assert_array_equal(g1[n], g2[n])
     assert rel(g1[0], g2[0]) < 1e-3 and rel(g1[3], g2[3]) < 1e-3
+
+
+@pytest.mark.parametrize("B,N,H,d", [(1, 5, 2, 128), (2, 129, 2, 64), (1, 300, 2, 128), (1, 640, 1, 64)])
+@pytest.mark.parametrize("from_j", [False, True])
+def test_noncausal_backward(B, N, H, d, from_j):
+    w = wl.Workload(f"bnc{B}x{N}x{H}x{d}", B, N, H, d, "bf16", seed=N * 5 + d, gate="head_uniform", lo=1.0,
+                    hi=5.0, bias_from_j=from_j, backward=True)
+    check_heads(w, non_causal=True)

@@ -27,23 +27,25 @@ def _gpu():
     fox.lib()  # fails loudly if the library is missing
 
 
-def run_fwd(w: wl.Workload, scale=0.0, arrays=None):
+def run_fwd(w: wl.Workload, scale=0.0, arrays=None, non_causal=False):
     import forget_gated_softmax_gb300 as fox
 
     arrays = arrays if arrays is not None else wl.draw(w, with_dO=False)
     t = to_torch(arrays, w.dtype)
     ws = fox.workspace(fox.fox_fwd_workspace_bytes(fox.make_params(w.B, w.N, w.H, w.d, 0 if w.dtype == "bf16" else 1,
-                                                                   scale, w.bias_from_j)), "cuda")
-    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], scale=scale, bias_from_j=w.bias_from_j, ws=ws)
+                                                                   scale, w.bias_from_j, non_causal)), "cuda")
+    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], scale=scale, bias_from_j=w.bias_from_j,
+                         non_causal=non_causal, ws=ws)
     assert fox.fox_check_error(ws) == 0
     torch.cuda.synchronize()
     return arrays, o, lse
 
 
-def check_full(w: wl.Workload, scale=0.0, arrays=None):
-    arrays, o, lse = run_fwd(w, scale, arrays)
+def check_full(w: wl.Workload, scale=0.0, arrays=None, non_causal=False):
+    arrays, o, lse = run_fwd(w, scale, arrays, non_causal)
     x = exact(arrays, w.dtype)
-    O_ref, L_ref = ora.forward(x["q"], x["k"], x["v"], x["z"], scale=scale or None, bias_from_j=w.bias_from_j)
+    O_ref, L_ref = ora.forward(x["q"], x["k"], x["v"], x["z"], scale=scale or None, bias_from_j=w.bias_from_j,
+                               causal=not non_causal)
     tol_o, tol_l = (TOL_O_BF16, TOL_LSE_BF16) if w.dtype == "bf16" else (TOL_O_F32, TOL_LSE_F32)
     err_o = o_excess_error(tensor_f64(o), O_ref, w.dtype)
     err_l = np.abs(tensor_f64(lse) - L_ref).max()
@@ -157,3 +159,21 @@ def test_outputs_leave_neighbours_untouched():
     assert torch.isnan(obuf[:G]).all() and torch.isnan(obuf[-G:]).all()
     assert torch.isnan(lbuf[:G]).all() and torch.isnan(lbuf[-G:]).all()
     assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
+@pytest.mark.parametrize("B,N,H,d", [(1, 1, 1, 64), (2, 129, 2, 128), (1, 300, 3, 64), (1, 700, 2, 128)])
+@pytest.mark.parametrize("from_j", [False, True])
+def test_noncausal_forward(B, N, H, d, from_j):
+    """The module's encoder mode: every key, the outer-difference bias positive for keys after the query."""
+    w = wl.Workload(f"nc{B}x{N}x{H}x{d}", B, N, H, d, "bf16", seed=N + 3 * d, gate="head_uniform", lo=0.0,
+                    hi=5.0, bias_from_j=from_j)
+    check_full(w, non_causal=True)
+
+
+def test_noncausal_fp32_is_unsupported():
+    import forget_gated_softmax_gb300 as fox
+
+    t = to_torch(wl.draw(wl.Workload("ncf", 1, 64, 1, 64, "f32", seed=1)), "f32")
+    with pytest.raises(fox.FoxError) as e:
+        fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], non_causal=True)
+    assert e.value.status == 2

@@ -13,6 +13,9 @@ Sources (web pages, cited by title and section):
                 and "ALiBi is the zero-variance limit".
   [foxwindow-len] foxwindow README, "The window is a first-passage time"
                 (the epsilon-effective window) and "An exact two-moment law".
+  [foxwindow-mono] foxwindow README, "The window is a first-passage time":
+                every log f_t < 0, so the bias falls monotonically with the
+                distance i - j (the basis of the tile-skip bound below).
   [fast-tf]     fast-transformers "Creating a custom attention layer",
                 section "New Attention" (inputs already projected and split
                 into heads; einsum layout "nlhe,nshe->nhls", i.e. [B, N, H, d]).
@@ -54,7 +57,21 @@ __all__ = [
     "gate_grad_bruteforce",
     "default_scale",
     "effective_window",
+    "tile_pair_bound",
+    "tile_pair_excess",
+    "tile_span",
+    "SKIP_THRESHOLD_LOG2",
 ]
+
+# A causal (query tile, key tile) pair is skipped when the bound below says
+# every weight in it is under 2^-150 of its row's largest weight. 2^-150 is
+# past the smallest subnormal fp32 (2^-149); an fp32 exponential that flushes
+# subnormals returns exactly 0 below 2^-126, so the 24 binary orders between
+# the two cover the rounding of the quantities the bound is formed from.
+SKIP_THRESHOLD_LOG2 = 150.0
+
+
+LOG2E = 1.0 / math.log(2.0)
 
 
 def default_scale(d: int) -> float:
@@ -277,3 +294,89 @@ def effective_window(z, eps: float, rows=None) -> np.ndarray:
                 out[o] = n
                 break
     return out
+
+
+def _column_term(c: np.ndarray, a: np.ndarray, bias_from_j: bool) -> np.ndarray:
+    """The key-side term of D: D_ij = c_i - colterm_j [FoX-module, forward()]:
+    colterm_j = c_j (j+1 convention) or c_{j-1} = c_j - a_j (j convention)."""
+    return c - a if bias_from_j else c
+
+
+def tile_pair_bound(q, k, z, scale=None, bias_from_j=False, tile=128) -> np.ndarray:
+    """Upper bound U[I, J] (log2 units) on x_ij - M_i over query tile I and key tile J < I
+    of one head (q, k [N, d], z [N]); +inf where J >= I. x_ij = (scale q_i.k_j + D_ij) log2 e
+    and M_i = max_{j<=i} x_ij is the row's largest causal logit.
+
+    [foxwindow-mono]: a_t <= 0, so colterm_t is non-increasing in t. With i in
+    tile I (i >= i0, its first row) and j in tile J (j <= j1, its last key),
+        x_ij - M_i <= x_ij - x_ii = scale log2e (q_i.k_j - q_i.k_i) + (colterm_i - colterm_j) log2e
+                   <= |scale| log2e qmax_I (kmax_J + kmax_I) + (colterm_{i0} - colterm_{j1}) log2e
+    (Cauchy-Schwarz on both dot products; qmax_T, kmax_T = largest row norm of q, k
+    in tile T). kmax_J is replaced by the largest kmax over tiles 0..J, which keeps the
+    bound valid and makes it non-increasing as J moves back from the diagonal."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    a = log_forget_gate(z)
+    colterm = _column_term(cumulative_log_gate(a), a, bias_from_j)
+    nT = (N + tile - 1) // tile
+    qn = np.sqrt((q * q).sum(axis=1))
+    kn = np.sqrt((k * k).sum(axis=1))
+    qmax = np.array([qn[T * tile:(T + 1) * tile].max() for T in range(nT)])
+    kmax = np.array([kn[T * tile:(T + 1) * tile].max() for T in range(nT)])
+    kpre = np.maximum.accumulate(kmax)
+    s2 = abs(scale) * LOG2E
+    U = np.full((nT, nT), np.inf)
+    for I in range(nT):
+        for J in range(I):
+            U[I, J] = s2 * qmax[I] * (kpre[J] + kmax[I]) + (colterm[I * tile] - colterm[J * tile + tile - 1]) * LOG2E
+    return U
+
+
+def tile_pair_excess(q, k, z, scale=None, bias_from_j=False, tile=128) -> np.ndarray:
+    """The exact quantity tile_pair_bound bounds: E[I, J] = max over rows i (< N) of
+    tile I and keys j of tile J with j <= i of x_ij - M_i (log2 units), from the full
+    fp64 logits of attention_head; -inf where the pair holds no causal entry. Brute
+    force; for tests."""
+    q = np.asarray(q, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    D = forget_bias(log_forget_gate(z), bias_from_j)
+    X = (scale * (q @ np.asarray(k, np.float64).T) + D) * LOG2E
+    X[np.triu(np.ones((N, N), dtype=bool), k=1)] = -np.inf
+    M = X.max(axis=1)
+    nT = (N + tile - 1) // tile
+    E = np.full((nT, nT), -np.inf)
+    for I in range(nT):
+        rows = slice(I * tile, min(N, (I + 1) * tile))
+        for J in range(I + 1):
+            cols = slice(J * tile, min(N, (J + 1) * tile))
+            E[I, J] = (X[rows, cols] - M[rows, None]).max()
+    return E
+
+
+def tile_span(q, k, z, scale=None, bias_from_j=False, tile=128, threshold=SKIP_THRESHOLD_LOG2):
+    """Key-tile span of every query tile under the tile-skip rule, one head.
+
+    Pair (I, J), J < I, is negligible when tile_pair_bound U[I, J] < -threshold.
+    U is non-increasing as J moves back from the diagonal, so the negligible key tiles
+    of query tile I are J < jraw(I) (jraw(I) = 0 if there are none). To give every key
+    tile a contiguous range of query tiles, the start is made non-decreasing in I:
+        jmin(I) = min_{I' >= I} jraw(I')   (this only keeps more pairs than jraw does),
+        imax(J) = max{ I : jmin(I) <= J }  (>= J, since jmin(J) <= J).
+    Query tile I then visits key tiles jmin(I)..I and key tile J serves query tiles
+    J..imax(J). Returns (jmin, imax), int64 [nT] each."""
+    U = tile_pair_bound(q, k, z, scale, bias_from_j, tile)
+    nT = U.shape[0]
+    jraw = np.zeros(nT, dtype=np.int64)
+    for I in range(nT):
+        for J in range(I - 1, -1, -1):
+            if U[I, J] < -threshold:
+                jraw[I] = J + 1
+                break
+    jmin = np.minimum.accumulate(jraw[::-1])[::-1].copy()
+    imax = np.array([max(I for I in range(nT) if jmin[I] <= J) for J in range(nT)], dtype=np.int64)
+    return jmin, imax

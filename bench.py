@@ -232,6 +232,28 @@ def max_over_ranks(value: float, dist=None, device="cpu") -> float:
     return float(t.item())
 
 
+def timed_variant(fox, torch, stream, fn, steps: int, flops: float) -> dict:
+    """Warm up, then time `steps` calls of fn on `stream` with CUDA events and the
+    library trace; returns ms per step, nominal TFLOP/s and per-kernel totals."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fox.trace_begin()
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    rec = fox.trace_end()
+    ms = a.elapsed_time(b) / steps
+    per = {}
+    for name, t in rec:
+        per[name] = per.get(name, 0.0) + t / steps
+    return {"ms_per_step": ms, "tflops_nominal": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "kernel_ms_per_step": per, "launches_per_step": len(rec) // steps}
+
+
 def run_fox(args, rank: int, world: int, local_rank: int):
     import torch
 
@@ -387,6 +409,35 @@ def run_fox(args, rank: int, world: int, local_rank: int):
         "frac": w_bytes / (w_ms * 1e-3) / 1e9 / measured_peaks()[0]["hbm_gbs"],
         "rows_passing": int((win >= 0).sum().item()),
     }
+
+    # Decay-aware tile skipping (causal, bit-identical outputs): the same step with
+    # tile_skip = 1, on the same inputs; nominal FLOPs over its time is the effective rate.
+    ps = fox.make_params(w.B, w.N, w.H, w.d, 0, 0.0, False, tile_skip=True)
+    ws_sf = fox.workspace(fox.fox_fwd_workspace_bytes(ps), "cuda")
+    ws_sb = fox.workspace(fox.fox_bwd_workspace_bytes(ps), "cuda")
+
+    def skip_step():
+        fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_sf, stream=stream, tile_skip=True)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_sb, stream=stream, tile_skip=True)
+
+    extra["tile_skip"] = timed_variant(fox, torch, stream, skip_step, 10, w.fwd_flops() + w.bwd_flops())
+    assert fox.fox_check_error(ws_sf) == 0 and fox.fox_check_error(ws_sb) == 0, "device-side error"
+    jmin, _ = fox.fox_tile_span(q, k, z, stream=stream)
+    nT = jmin.shape[1]
+    visited = (torch.arange(nT, device="cuda")[None, :] - jmin + 1).sum().item()
+    extra["tile_skip"]["pairs_visited_frac"] = visited / (w.B * w.H * nT * (nT + 1) / 2)
+    extra["tile_skip"]["speedup_vs_full_step"] = (elapsed_ms / args.steps) / extra["tile_skip"]["ms_per_step"]
+
+    # Non-causal (encoder) mode on the same inputs: every key for every query.
+    def nc_step():
+        fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_f, stream=stream, non_causal=True)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream, non_causal=True)
+
+    nc_flops = 2 * (w.fwd_flops() + w.bwd_flops())  # the full N^2 score matrix instead of its causal half
+    extra["non_causal"] = timed_variant(fox, torch, stream, nc_step, 5, nc_flops)
+    extra["non_causal"]["note"] = ("flops: 4BHN^2d forward + 10BHN^2d backward; the backward also re-runs the "
+                                   "forward once with a two-term P to form Delta")
+    assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

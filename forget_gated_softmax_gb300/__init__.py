@@ -46,6 +46,7 @@ EXPORTS = (
     "fox_noalloc_scratch_bytes",
     "fox_window",
     "fox_window_workspace_bytes",
+    "fox_tile_span",
 )
 
 
@@ -65,6 +66,7 @@ class fox_params(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("bias_from_j", ctypes.c_int),
         ("non_causal", ctypes.c_int),
+        ("tile_skip", ctypes.c_int),
     ]
 
 
@@ -105,6 +107,8 @@ def lib() -> ctypes.CDLL:
         L.fox_window_workspace_bytes.restype = sz
         L.fox_window.argtypes = [pp, vp, ctypes.c_double, vp, vp, sz, vp]
         L.fox_window.restype = i
+        L.fox_tile_span.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.fox_tile_span.restype = i
         L.fox_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp]
         L.fox_fwd_noalloc.restype = i
         L.fox_noalloc_scratch_bytes.argtypes = []
@@ -124,9 +128,10 @@ def fox_status_string(status: int) -> str:
         return STATUS_NAMES.get(int(status), f"status {status}")
 
 
-def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False, non_causal=False) -> fox_params:
+def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False, non_causal=False,
+                tile_skip=False) -> fox_params:
     return fox_params(int(B), int(N), int(H), int(d), int(dtype), float(scale), int(bool(bias_from_j)),
-                      int(bool(non_causal)))
+                      int(bool(non_causal)), int(bool(tile_skip)))
 
 
 def fox_fwd_workspace_bytes(params: fox_params) -> int:
@@ -178,6 +183,7 @@ def fox_fwd(
     scale: float = 0.0,
     bias_from_j: bool = False,
     non_causal: bool = False,
+    tile_skip: bool = False,
     o=None,
     lse=None,
     ws=None,
@@ -190,7 +196,7 @@ def fox_fwd(
     """
     torch = _torch()
     B, N, H, d = q.shape
-    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal)
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal, tile_skip)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
@@ -221,6 +227,7 @@ def fox_bwd(
     scale: float = 0.0,
     bias_from_j: bool = False,
     non_causal: bool = False,
+    tile_skip: bool = False,
     dq=None,
     dk=None,
     dv=None,
@@ -231,7 +238,7 @@ def fox_bwd(
     """Backward (bf16): returns (dQ, dK, dV, dz); dz is fp32 [B, N, H]."""
     torch = _torch()
     B, N, H, d = q.shape
-    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal)
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal, tile_skip)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -288,6 +295,27 @@ def fox_window(z, eps: float, *, window=None, ws=None, stream=None):
     if st != 0:
         raise FoxError(st, "fox_window")
     return window
+
+
+def fox_tile_span(q, k, z, *, scale: float = 0.0, bias_from_j: bool = False, ws=None, stream=None):
+    """Tile spans of the decay-aware tile skip: (jmin, imax), int32 [B*H, ceil(N/128)] each
+    (first key tile of every query tile, last query tile of every key tile)."""
+    torch = _torch()
+    B, N, H, d = q.shape
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, tile_skip=True)
+    nT = (N + 127) // 128
+    jmin = torch.empty((B * H, nT), dtype=torch.int32, device=q.device)
+    imax = torch.empty((B * H, nT), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(fox_fwd_workspace_bytes(params), q.device)
+    for t in (q, k, z):
+        if not t.is_contiguous():
+            raise ValueError("fox_tile_span needs contiguous tensors")
+    st = lib().fox_tile_span(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(z), _ptr(jmin), _ptr(imax), _ptr(ws),
+                             ws.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_tile_span")
+    return jmin, imax
 
 
 def fox_check_error(ws, stream=None) -> int:

@@ -102,8 +102,10 @@ fox_status check_params(const fox_params* p) {
   if (p->dtype != FOX_DTYPE_BF16 && p->dtype != FOX_DTYPE_F32) return FOX_ERR_INVALID_ARG;
   if (p->bias_from_j != 0 && p->bias_from_j != 1) return FOX_ERR_INVALID_ARG;
   if (p->non_causal != 0 && p->non_causal != 1) return FOX_ERR_INVALID_ARG;
+  if (p->tile_skip != 0 && p->tile_skip != 1) return FOX_ERR_INVALID_ARG;
   if (!(p->scale >= 0.f) || std::isinf(p->scale)) return FOX_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return FOX_ERR_UNSUPPORTED;
+  if (p->tile_skip && (p->non_causal || p->dtype != FOX_DTYPE_BF16)) return FOX_ERR_UNSUPPORTED;
   const long long BH = (long long)p->B * p->H;
   if (BH > kMaxTokens || (long long)p->N > kMaxTokens - 2 * kTile) return FOX_ERR_INVALID_ARG;
   if (BH * (long long)p->N > kMaxTokens) return FOX_ERR_INVALID_ARG;
@@ -129,7 +131,7 @@ const char* fox_status_string(fox_status s) {
   switch (s) {
     case FOX_OK: return "FOX_OK";
     case FOX_ERR_INVALID_ARG: return "FOX_ERR_INVALID_ARG: invalid argument (null pointer, size, alignment or flag)";
-    case FOX_ERR_UNSUPPORTED: return "FOX_ERR_UNSUPPORTED: head dimension or dtype not implemented";
+    case FOX_ERR_UNSUPPORTED: return "FOX_ERR_UNSUPPORTED: head dimension, dtype or flag combination not implemented";
     case FOX_ERR_WORKSPACE: return "FOX_ERR_WORKSPACE: workspace null, misaligned or too small";
     case FOX_ERR_CUDA: return "FOX_ERR_CUDA: a CUDA call or kernel launch failed";
     case FOX_ERR_TIMEOUT: return "FOX_ERR_TIMEOUT: a device-side wait gave up";
@@ -164,6 +166,9 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  if (p->tile_skip &&
+      launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
 
   char* ws = static_cast<char*>(workspace);
   AttnFwdArgs a;
@@ -181,6 +186,7 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
   a.colrec = reinterpret_cast<const float*>(ws + g.colrec);
   a.err = reinterpret_cast<uint32_t*>(ws);
   a.non_causal = p->non_causal;
+  if (p->tile_skip) a.jmin = reinterpret_cast<const int*>(ws + g.jmin);
   if (p->dtype == FOX_DTYPE_F32) {
     if (p->non_causal) return FOX_ERR_UNSUPPORTED;
     if (p->B * p->H > 65535) return FOX_ERR_UNSUPPORTED;
@@ -211,6 +217,9 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   if (st != FOX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  if (p->tile_skip &&
+      launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
   CUtensorMap maps[4];
   if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d, 64) ||
       !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d, kTile) ||
@@ -237,6 +246,7 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   a.dv = dv;
   a.dz = dz;
   a.ws = static_cast<char*>(workspace);
+  if (p->tile_skip) a.imax = reinterpret_cast<const int*>(a.ws + g.imax);
   if (p->non_causal) {
     // Without the causal mask the gate gradient is a small difference of large
     // row and column sums of dS = P (dP - Delta), and a Delta_i = dO_i . O_i
@@ -269,6 +279,30 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
     a.delta_ready = 1;
   }
   return launch_attn_bwd(a, g, w, maps, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
+}
+
+fox_status fox_tile_span(const fox_params* p, const void* q, const void* k, const float* z, int32_t* jmin,
+                         int32_t* imax, void* workspace, size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (p->dtype != FOX_DTYPE_BF16 || p->non_causal) return FOX_ERR_UNSUPPORTED;
+  if (empty_problem(p)) return FOX_OK;
+  if (!q || !k || !z || !jmin || !imax) return FOX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(z, 4) || !aligned(jmin, 4) || !aligned(imax, 4))
+    return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  st = check_workspace(workspace, workspace_bytes, g.end);
+  if (st != FOX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  if (launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
+  const char* ws = static_cast<const char*>(workspace);
+  const size_t bytes = sizeof(int32_t) * (size_t)g.BH * g.nT;
+  if (cudaMemcpyAsync(jmin, ws + g.jmin, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(imax, ws + g.imax, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
+  return FOX_OK;
 }
 
 size_t fox_window_workspace_bytes(const fox_params* p) {

@@ -114,6 +114,7 @@ struct BwdKParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   uint32_t* err;
+  const int* imax;  // tile skipping: last query tile of each key tile ([bh][nT]), or null
 };
 
 constexpr int kHalf = 64;        // queries per half-tile
@@ -247,10 +248,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int J = static_cast<int>(blockIdx.x) / BH;  // key tile; J = 0 has the most query tiles
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.H, h = bh % p.H;
-  // Half-tiles of 64 queries: causal, query tiles I = J .. nT-1; non-causal, all of them.
+  // Half-tiles of 64 queries: causal, query tiles I = J .. nT-1 (.. imax(J) with tile
+  // skipping); non-causal, all of them.
   const bool causal = !p.non_causal;
   const int I_first = causal ? J : 0;
-  const int G = 2 * (p.nT - I_first);
+  const int I_last = p.imax ? p.imax[(size_t)bh * p.nT + J] : p.nT - 1;
+  const int G = 2 * (I_last - I_first + 1);
+  // The elementwise and readout warps read the half-tile count from shared memory at
+  // each iteration instead of holding it in a register (their register budget is full).
+  volatile int* G_shared = reinterpret_cast<volatile int*>(sm + L::kMisc + 8);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[BB_KV], 1);
@@ -266,6 +272,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars[BB_FINAL], 1);
     *abort_flag = 0;
+    *G_shared = G;
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T, query of R, key of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     bool ok = true;
-    for (int g = 0; g < G && ok; ++g) {
+    for (int g = 0; g < *G_shared && ok; ++g) {
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const int q0 = I_first * kTile + g * kHalf;
@@ -431,7 +438,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
     const float baseJ_hi = ok ? rec[kTile] : 0.f, baseJ_lo = ok ? rec[kTile + 1] : 0.f;
-    for (int g = 0; g < G && ok; ++g) {
+    for (int g = 0; g < *G_shared && ok; ++g) {
       const int x = g & 1, st = g % kStages;
       const int I = I_first + (g >> 1), half = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
@@ -639,6 +646,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = err;
+  p.imax = a.imax;
   const long long blocks = (long long)g.nT * g.BH;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {

@@ -55,6 +55,7 @@ struct FwdKParams {
   __nv_bfloat16* o;
   float* lse;
   uint32_t* err;
+  const int* jmin;  // tile skipping: first key tile of each query tile ([bh][nT]), or null
   // Delta mode (used by the non-causal backward): instead of O and LSE, write
   // delta[bh][i] = dO_i . O_i with O_i from the fp32 accumulator of a P V
   // product whose P is split into two bf16 terms.
@@ -219,12 +220,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for s >= first_k. Causal: the stream starts at the last diagonal tile and
   // tile k's first tile is its own diagonal. Non-causal: every tile, from the
   // last one back (the bias c_i - c_j grows with j, so the largest bias comes first).
+  // With tile skipping (causal only), tile k stops at key tile jmin(I_k): it takes
+  // part for first_k <= s < end_k.
   const int I0 = 2 * qb, I1 = 2 * qb + 1;
   const bool has1 = I1 < p.nT;
   const bool causal = !p.non_causal;
   const int Jtop = causal ? (has1 ? I1 : I0) : p.nT - 1;
-  const int nJ = Jtop + 1;
   const int first0 = (causal && has1) ? 1 : 0;
+  const int jm0 = p.jmin ? p.jmin[(size_t)bh * p.nT + I0] : 0;
+  const int jm1 = (p.jmin && has1) ? p.jmin[(size_t)bh * p.nT + I1] : 0;
+  const int end0 = Jtop - jm0 + 1;
+  const int end1 = has1 ? Jtop - jm1 + 1 : 0;
+  const int nJ = end0 > end1 ? end0 : end1;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q], 1);
@@ -301,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ[2] = {smem_u32(sm + L::kQ0), smem_u32(sm + L::kQ1)};
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
       const int first[2] = {first0, 0};
+      const int end[2] = {end0, end1};
       const bool active[2] = {true, has1};
       auto issue_s = [&](int k, int st) {
 #pragma unroll
@@ -349,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
         for (int k = 0; k < 2 && ok; ++k) {
           if (!active[k]) continue;
-          if (s >= first[k]) {
+          if (s >= first[k] && s < end[k]) {
             ok = mbar_wait(&bars[B_PFULL + k], (s - first[k]) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
             if (!ok) break;
             tc_fence_after();
             issue_pv(k, st, s > first[k]);
-            if (s + 1 < nJ) {
+            if (s + 1 < end[k]) {
               if (!(ok = wait_next_k())) break;
               issue_s(k, nst);
               umma_commit(&bars[B_SFULL + k]);
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;   // row within the Q tile
     const int I = k ? I1 : I0;
     const int first = k ? 0 : first0;
-    const int nJk = (k == 1 && !has1) ? 0 : (causal ? I + 1 : p.nT);
+    const int nJk = (k == 1 && !has1) ? 0 : (k ? end1 : end0 - first0);
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tbase + k * 128 + lane_off;
     const uint32_t tO = tbase + 256 + k * D + lane_off;
@@ -541,6 +549,7 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.err = a.err;
+  p.jmin = a.jmin;
   const long long blocks = (long long)p.nQB * a.B * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {

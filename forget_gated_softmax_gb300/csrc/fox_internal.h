@@ -21,9 +21,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 //                     base_T hi, base_T lo, 0, 0 },  base_T = sum_{l < 128*T} a_l (fp64 scan, split hi+lo)
 //   tiletot[bh][T]  sum of a over tile T (fp32, scratch between the two gate kernels)
 // so that, for i in tile I and j in tile J, D_ij * log2 e = l_i - kappa_j + (base_I - base_J).
+// Tile-skip arrays (written only when skipping is requested):
+//   qmax, kmax [bh][T]  largest row norm of q, k in tile T (fp32)
+//   kpre       [bh][T]  running maximum of kmax over tiles 0..T
+//   jmin       [bh][I]  first key tile query tile I visits (int)
+//   imax       [bh][J]  last query tile key tile J serves (int)
 struct GateLayout {
   int BH = 0, N = 0, nT = 0, Npad = 0;
-  size_t rowloc = 0, colrec = 0, tiletot = 0, end = 0;  // byte offsets from the workspace base
+  size_t rowloc = 0, colrec = 0, tiletot = 0;  // byte offsets from the workspace base
+  size_t qmax = 0, kmax = 0, kpre = 0, jmin = 0, imax = 0;
+  size_t end = 0;
 };
 
 // Backward-only buffers that follow the gate buffers.
@@ -52,7 +59,18 @@ inline GateLayout gate_layout(int B, int N, int H) {
   g.colrec = off;
   off = align_up(off + sizeof(float) * (size_t)g.BH * g.nT * kColRec, 256);
   g.tiletot = off;
-  off = align_up(off + sizeof(float) * (size_t)g.BH * g.nT, 256);
+  const size_t per_tile = sizeof(float) * (size_t)g.BH * g.nT;  // sizeof(int) == sizeof(float)
+  off = align_up(off + per_tile, 256);
+  g.qmax = off;
+  off = align_up(off + per_tile, 256);
+  g.kmax = off;
+  off = align_up(off + per_tile, 256);
+  g.kpre = off;
+  off = align_up(off + per_tile, 256);
+  g.jmin = off;
+  off = align_up(off + per_tile, 256);
+  g.imax = off;
+  off = align_up(off + per_tile, 256);
   g.end = off;
   return g;
 }
@@ -102,6 +120,7 @@ struct AttnFwdArgs {
   const float* rowloc;
   const float* colrec;
   uint32_t* err;
+  const int* jmin = nullptr;  // tile skipping: first key tile of each query tile ([bh][nT]), or null
   // When delta_out is set, the kernel writes delta_out[bh][i] = dO_i . O_i (O in fp32)
   // instead of O and LSE (rows i < N; layout [BH][Npad]).
   const void* dO_for_delta = nullptr;
@@ -131,6 +150,7 @@ struct AttnBwdArgs {
   // Set when Delta of rows i < N is already in the backward layout (the forward
   // kernel's Delta epilogue wrote it); the row kernel then only writes the padding.
   int delta_ready = 0;
+  const int* imax = nullptr;  // tile skipping: last query tile of each key tile ([bh][nT]), or null
 };
 
 // Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ
@@ -138,6 +158,11 @@ struct AttnBwdArgs {
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w,
                             const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box) */,
                             cudaStream_t s);
+
+// Decay-aware tile skipping: per-tile norms of q and k, then the key-tile span of every
+// query tile (jmin) and the query-tile span of every key tile (imax); needs the gate scan.
+cudaError_t launch_tile_span(const void* q, const void* k, int B, int N, int H, int d, float scale,
+                             const GateLayout& g, void* ws, cudaStream_t s);
 
 // Epsilon-effective window per query row (fp64 prefix scan + binary search).
 cudaError_t launch_window(const float* z, int B, int N, int H, double eps, int* out, void* ws, cudaStream_t s);

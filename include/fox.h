@@ -52,7 +52,8 @@ extern "C" {
 typedef enum fox_status {
   FOX_OK = 0,
   FOX_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, bad flag or dtype */
-  FOX_ERR_UNSUPPORTED = 2, /* well-formed but not implemented (d not in {64, 128}; fp32 backward) */
+  FOX_ERR_UNSUPPORTED = 2, /* well-formed but not implemented (d not in {64, 128}; fp32 backward;
+                              non_causal or tile_skip with fp32; tile_skip with non_causal) */
   FOX_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than the size query */
   FOX_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   FOX_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (from fox_check_error) */
@@ -72,6 +73,11 @@ typedef struct fox_params {
   int non_causal;  /* 0: causal (the module's "decoder" mode, the default); 1: every key, the module's
                       "encoder" mode, where the same outer difference D_ij = c_i - c_j (positive for
                       j > i) biases keys after the query too. bf16 forward and backward only. */
+  int tile_skip;   /* 0: visit every causal tile pair (default). 1: skip the (query tile, key tile)
+                      pairs whose every weight the decay bound puts below 2^-150 of its row's
+                      largest (see fox_tile_span); outputs are bit-identical to tile_skip = 0 for
+                      the forward, dK and dV, and equal up to the order of fp32 atomic sums for dQ
+                      and dz. Causal bf16 only (FOX_ERR_UNSUPPORTED otherwise). */
 } fox_params;
 
 /* Workspace bytes fox_fwd / fox_bwd need for these params (0 if params are invalid). */
@@ -118,6 +124,31 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
 size_t fox_window_workspace_bytes(const fox_params* p);
 fox_status fox_window(const fox_params* p, const float* z, double eps, int32_t* window, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/*
+ * Tile spans of the decay-aware tile skip (tile_skip = 1). The bias falls
+ * monotonically with distance because every log f_t < 0 (foxwindow README,
+ * "The window is a first-passage time"). So for query tile I (rows
+ * 128I..128I+127) and an earlier key tile J, in log2 units,
+ *   U(I,J) = scale log2e qmax_I (kmax_{<=J} + kmax_I) + (colterm(128I) - colterm(128J+127)) log2e
+ * bounds x_ij - max_j' x_ij' over the pair. Here:
+ *   - qmax_T, kmax_T are the largest row norms of q, k in tile T;
+ *   - kmax_{<=J} is the largest kmax over tiles 0..J;
+ *   - colterm(t) = c_t, or c_{t-1} when bias_from_j = 1.
+ * Pairs with U < -150 are skipped. Every weight in such a pair is then
+ * below 2^-150 of its row's largest, and the kernels' flushing exp2 makes it
+ * exactly 0. Outputs, int32 [B*H][nT] with nT = ceil(N/128):
+ *   jmin[bh][I]  first key tile that query tile I visits. It is made
+ *                non-decreasing in I by a suffix minimum, which only keeps
+ *                more pairs.
+ *   imax[bh][J]  last query tile that key tile J serves:
+ *                the largest I with jmin[bh][I] <= J.
+ * q, k: [B,N,H,d] bf16; z: [B,N,H] fp32; causal bf16 params only.
+ * Workspace: fox_fwd_workspace_bytes(p). jmin and imax are device pointers,
+ * written by stream-ordered copies.
+ */
+fox_status fox_tile_span(const fox_params* p, const void* q, const void* k, const float* z, int32_t* jmin,
+                         int32_t* imax, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Forward without a caller-provided workspace, for callers that cannot

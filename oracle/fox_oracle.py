@@ -61,6 +61,7 @@ __all__ = [
     "tile_pair_excess",
     "tile_span",
     "SKIP_THRESHOLD_LOG2",
+    "gate_projection",
 ]
 
 # A causal (query tile, key tile) pair is skipped when the bound below says
@@ -77,6 +78,19 @@ LOG2E = 1.0 / math.log(2.0)
 def default_scale(d: int) -> float:
     """d^-1/2 [FoX-module, __init__: scale = head_dim ** -0.5]."""
     return float(d) ** -0.5
+
+
+def gate_projection(x, w_f, b_f) -> np.ndarray:
+    """Gate logits z = x W_f^T + b_f, x [..., hidden] -> z [..., H], in fp64.
+
+    [FoX-module, __init__: f_proj = Linear(hidden_size, num_heads, bias=True);
+    forward(): f = sigmoid(f_proj(x))]. The Linear's weight is laid out
+    [out_features, in_features] = [H, hidden]; this returns its pre-sigmoid
+    output, the z every other function here takes. A library matmul is the step.
+    """
+    x = np.asarray(x, np.float64)
+    w_f = np.asarray(w_f, np.float64)
+    return x @ w_f.T + np.asarray(b_f, np.float64)
 
 
 def log_forget_gate(z) -> np.ndarray:

@@ -400,3 +400,26 @@ def test_noncausal_rows_variant_matches_whole_head():
     Or, lr = ora.attention_rows(q, k, v, z, rows, causal=False)
     np.testing.assert_allclose(Or, O[rows], atol=1e-12)
     np.testing.assert_allclose(lr, lse[rows], atol=1e-12)
+
+
+# ----------------------------------------------------------------- gate projection
+def test_gate_projection_is_torch_linear():
+    """z = f_proj(x) with f_proj = nn.Linear(hidden, H, bias=True): the library routine in fp64."""
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((2, 7, 48))
+    w = rng.standard_normal((5, 48))
+    b = rng.standard_normal(5)
+    ref = torch.nn.functional.linear(torch.tensor(x), torch.tensor(w), torch.tensor(b)).numpy()
+    np.testing.assert_allclose(ora.gate_projection(x, w, b), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_gate_projection_special_inputs():
+    """One-hot rows pick weight columns (so the weight layout is [H, hidden], not its
+    transpose); x = 0 gives the bias alone."""
+    rng = np.random.default_rng(41)
+    hidden, H = 12, 3
+    w = rng.standard_normal((H, hidden))
+    b = rng.standard_normal(H)
+    x = np.eye(hidden)[None]
+    np.testing.assert_array_equal(ora.gate_projection(x, w, b)[0], w.T + b)
+    np.testing.assert_array_equal(ora.gate_projection(np.zeros((1, 4, hidden)), w, b)[0], np.tile(b, (4, 1)))

@@ -71,3 +71,18 @@ def test_native_generator_matches_numpy_definition():
     np.testing.assert_array_equal(u, wl.splitmix64(11, 1000, 64))
     for start, count in ((0, 1), (6, 100001), (1 << 33, 4097)):
         np.testing.assert_array_equal(wl.normals_f32(9, start, count), wl.normals(9, start, count).astype(np.float32))
+
+
+def test_gate_projection_inputs():
+    """Shapes, bf16 patterns, determinism, and z = x W^T + b near the recipe's b_h + N(0, sigma^2)."""
+    w = wl.Workload("proj", 2, 300, 4, 64, "bf16", 7, gate="head_linspace", lo=0.0, hi=3.0, sigma=0.5)
+    a = wl.draw_gate_projection(w, 256)
+    b = wl.draw_gate_projection(w, 256)
+    assert a["x"].shape == (2, 300, 256) and a["x"].dtype == np.uint16
+    assert a["w_f"].shape == (4, 256) and a["w_f"].dtype == np.uint16
+    assert a["b_f"].dtype == np.float32
+    for n in a:
+        np.testing.assert_array_equal(a[n], b[n])
+    np.testing.assert_allclose(a["b_f"], np.linspace(0.0, 3.0, 4), rtol=1e-6)
+    z = wl.bf16_bits_to_f64(a["x"]) @ wl.bf16_bits_to_f64(a["w_f"]).T
+    assert abs(z.mean()) < 0.05 and abs(z.std() - 0.5) < 0.05

@@ -209,6 +209,39 @@ def draw(w: Workload, with_dO: Optional[bool] = None):
     return out
 
 
+def gate_head_bias(w: Workload) -> np.ndarray:
+    """The per-head gate bias b_h of the "head_uniform" / "head_linspace" recipes (fp64 [H])."""
+    off = _offsets(w)
+    if w.gate == "head_uniform":
+        return w.lo + (w.hi - w.lo) * uniforms(w.seed, off["bh"], w.H)
+    if w.gate == "head_linspace":
+        return np.linspace(w.lo, w.hi, w.H) if w.H > 1 else np.array([w.lo])
+    raise ValueError(f"gate recipe {w.gate!r} has no per-head bias")
+
+
+PROJ_SEED_XOR = 0x6A09E667F3BCC908  # separate stream for the gate-projection inputs
+
+
+def draw_gate_projection(w: Workload, hidden: int):
+    """Synthetic inputs of the gate projection z = x W^T + b for workload `w`.
+
+    x [B, N, hidden] ~ N(0, 1) and W [H, hidden] ~ N(0, sigma^2 / hidden), both
+    rounded to bf16 (uint16 bit patterns); b [H] = the recipe's b_h (fp32). Then
+    z_h is about b_h + N(0, sigma^2) per token, the recipe's own gate distribution.
+    Drawn from their own SplitMix64 stream (seed ^ PROJ_SEED_XOR): x from output 0,
+    W right after it.
+    """
+    seed = (w.seed ^ PROJ_SEED_XOR) & 0xFFFFFFFFFFFFFFFF
+    nx = w.B * w.N * hidden
+    x = normals_f32(seed, 0, nx)
+    wt = normals_f32(seed, normal_outputs(nx), w.H * hidden) * np.float32(w.sigma / math.sqrt(hidden))
+    return {
+        "x": f32_to_bf16_bits(x).reshape(w.B, w.N, hidden),
+        "w_f": f32_to_bf16_bits(wt).reshape(w.H, hidden),
+        "b_f": gate_head_bias(w).astype(np.float32),
+    }
+
+
 def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     """Exact fp64 values of a drawn tensor (bf16 bit patterns are decoded)."""
     return bf16_bits_to_f64(x) if dtype == "bf16" else np.asarray(x, dtype=np.float64)

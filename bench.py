@@ -439,6 +439,27 @@ def run_fox(args, rank: int, world: int, local_rank: int):
                                    "forward once with a two-term P to form Delta")
     assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
 
+    # Gate projection fused with the gate scan (z = x W_f^T + b_f, hidden = H d): HBM-bound
+    # on reading x; timed alone and as part of the forward from x.
+    hidden = w.H * w.d
+    gp = wl.draw_gate_projection(w, hidden)
+    xg = torch.from_numpy(gp["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    wg = torch.from_numpy(gp["w_f"].view(np.int16)).view(torch.bfloat16).cuda()
+    bg = torch.from_numpy(gp["b_f"]).cuda()
+    zg = torch.empty_like(z)
+    gp_res = timed_variant(fox, torch, stream, lambda: fox.fox_gate_proj(xg, wg, bg, z=zg, ws=ws_f, stream=stream),
+                           20, 2.0 * w.tokens * hidden)
+    gp_ms = gp_res["kernel_ms_per_step"].get("gate_proj_scan", gp_res["ms_per_step"])
+    gp_bytes = w.B * w.N * hidden * 2 + w.H * hidden * 2 + w.tokens * (4 + 4 + 4 + 4)  # x, W in; z, gate terms out
+    extra["gate_projection"] = {
+        "hidden": hidden, "ms_per_call": gp_res["ms_per_step"], "kernel_ms": gp_ms,
+        "achieved": gp_bytes / (gp_ms * 1e-3) / 1e9, "unit": "GB/s", "bound": "hbm",
+        "frac": gp_bytes / (gp_ms * 1e-3) / 1e9 / measured_peaks()[0]["hbm_gbs"],
+        "kernel_ms_per_call": gp_res["kernel_ms_per_step"],
+    }
+    assert fox.fox_check_error(ws_f) == 0, "device-side error"
+    del xg
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, dt_cpu = oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)

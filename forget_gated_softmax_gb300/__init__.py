@@ -47,6 +47,8 @@ EXPORTS = (
     "fox_window",
     "fox_window_workspace_bytes",
     "fox_tile_span",
+    "fox_gate_proj",
+    "fox_fwd_xgate",
 )
 
 
@@ -107,6 +109,10 @@ def lib() -> ctypes.CDLL:
         L.fox_window_workspace_bytes.restype = sz
         L.fox_window.argtypes = [pp, vp, ctypes.c_double, vp, vp, sz, vp]
         L.fox_window.restype = i
+        L.fox_gate_proj.argtypes = [pp, i, vp, vp, vp, vp, vp, sz, vp]
+        L.fox_gate_proj.restype = i
+        L.fox_fwd_xgate.argtypes = [pp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.fox_fwd_xgate.restype = i
         L.fox_tile_span.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fox_tile_span.restype = i
         L.fox_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp]
@@ -295,6 +301,49 @@ def fox_window(z, eps: float, *, window=None, ws=None, stream=None):
     if st != 0:
         raise FoxError(st, "fox_window")
     return window
+
+
+def fox_gate_proj(x, w_f, b_f, *, bias_from_j: bool = False, z=None, ws=None, stream=None):
+    """Gate logits z = x W_f^T + b_f: x [B, N, hidden] bf16, W_f [H, hidden] bf16, b_f [H] fp32
+    -> z [B, N, H] fp32 (tensor cores; the gate scan runs in the same kernel into `ws`)."""
+    torch = _torch()
+    B, N, hidden = x.shape
+    H = w_f.shape[0]
+    params = make_params(B, N, H, 64, FOX_DTYPE_BF16, 0.0, bias_from_j)
+    if z is None:
+        z = torch.empty((B, N, H), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(fox_fwd_workspace_bytes(params), x.device)
+    for t in (x, w_f, b_f, z):
+        if not t.is_contiguous():
+            raise ValueError("fox_gate_proj needs contiguous tensors")
+    st = lib().fox_gate_proj(ctypes.byref(params), int(hidden), _ptr(x), _ptr(w_f), _ptr(b_f), _ptr(z), _ptr(ws),
+                             ws.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_gate_proj")
+    return z
+
+
+def fox_fwd_xgate(q, k, v, x, w_f, b_f, *, scale: float = 0.0, bias_from_j: bool = False, tile_skip: bool = False,
+                  z=None, o=None, lse=None, ws=None, stream=None):
+    """Forward from the gate projection: returns (O, LSE, z) with z = x W_f^T + b_f [B, N, H] fp32."""
+    torch = _torch()
+    B, N, H, d = q.shape
+    hidden = x.shape[-1]
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, tile_skip=tile_skip)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, N, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    z = torch.empty((B, N, H), dtype=torch.float32, device=q.device) if z is None else z
+    if ws is None:
+        ws = workspace(fox_fwd_workspace_bytes(params), q.device)
+    for t in (q, k, v, x, w_f, b_f, z, o, lse):
+        if not t.is_contiguous():
+            raise ValueError("fox_fwd_xgate needs contiguous tensors")
+    st = lib().fox_fwd_xgate(ctypes.byref(params), int(hidden), _ptr(q), _ptr(k), _ptr(v), _ptr(x), _ptr(w_f),
+                             _ptr(b_f), _ptr(z), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_fwd_xgate")
+    return o, lse, z
 
 
 def fox_tile_span(q, k, z, *, scale: float = 0.0, bias_from_j: bool = False, ws=None, stream=None):

@@ -45,6 +45,32 @@ bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_x_map(CUtensorMap* map, const void* base, int B, int N, int hidden) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)hidden, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)hidden * 2, (cuuint64_t)N * hidden * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_wf_map(CUtensorMap* map, const void* base, int H, int hidden) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)H};
+  const cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)((H + 15) / 16 * 16)};
+  const cuuint32_t estr[2] = {1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ tracing
 namespace {
 struct TraceRec {
@@ -151,25 +177,17 @@ size_t fox_bwd_workspace_bytes(const fox_params* p) {
   return bwd_layout(g, p->d).end;
 }
 
-fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
-                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  fox_status st = check_params(p);
-  if (st != FOX_OK) return st;
-  if (empty_problem(p)) return FOX_OK;
-  if (!q || !k || !v || !z || !o || !lse) return FOX_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(z, 4) ||
-      !aligned(lse, 4))
-    return FOX_ERR_INVALID_ARG;
-  const GateLayout g = gate_layout(p->B, p->N, p->H);
-  st = check_workspace(workspace, workspace_bytes, g.end);
-  if (st != FOX_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+}  // extern "C"
 
-  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+namespace {
+
+// The forward after the gate terms are in the workspace: tile spans (tile_skip), then the
+// attention kernel.
+fox_status fwd_after_gate(const fox_params* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* workspace, const GateLayout& g, cudaStream_t s) {
   if (p->tile_skip &&
       launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
     return FOX_ERR_CUDA;
-
   char* ws = static_cast<char*>(workspace);
   AttnFwdArgs a;
   a.B = p->B;
@@ -197,6 +215,72 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
       !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d))
     return FOX_ERR_CUDA;
   return launch_attn_fwd_bf16(a, maps, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
+}
+
+// Checks and the fused projection + scan shared by fox_gate_proj and fox_fwd_xgate.
+fox_status gate_proj(const fox_params* p, int hidden, const void* x, const void* w_f, const float* b_f, float* z,
+                     void* workspace, size_t workspace_bytes, const GateLayout& g, cudaStream_t s) {
+  if (p->dtype != FOX_DTYPE_BF16) return FOX_ERR_UNSUPPORTED;
+  if (hidden <= 0 || hidden % 8 != 0) return FOX_ERR_INVALID_ARG;
+  if (p->H > 256) return FOX_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->N * (long long)hidden > (1LL << 40)) return FOX_ERR_INVALID_ARG;
+  if (!x || !w_f || !b_f) return FOX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_f, 16) || !aligned(b_f, 4) || (z && !aligned(z, 4))) return FOX_ERR_INVALID_ARG;
+  fox_status st = check_workspace(workspace, workspace_bytes, g.end);
+  if (st != FOX_OK) return st;
+  CUtensorMap maps[2];
+  if (!make_x_map(&maps[0], x, p->B, p->N, hidden) || !make_wf_map(&maps[1], w_f, p->H, hidden)) return FOX_ERR_CUDA;
+  return launch_gate_proj_scan(maps, b_f, hidden, z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) ==
+                 cudaSuccess
+             ? FOX_OK
+             : FOX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (empty_problem(p)) return FOX_OK;
+  if (!q || !k || !v || !z || !o || !lse) return FOX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(z, 4) ||
+      !aligned(lse, 4))
+    return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  st = check_workspace(workspace, workspace_bytes, g.end);
+  if (st != FOX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  return fwd_after_gate(p, q, k, v, o, lse, workspace, g, s);
+}
+
+fox_status fox_gate_proj(const fox_params* p, int hidden, const void* x, const void* w_f, const float* b_f, float* z,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (empty_problem(p)) return FOX_OK;
+  if (!z) return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  return gate_proj(p, hidden, x, w_f, b_f, z, workspace, workspace_bytes, g, static_cast<cudaStream_t>(stream));
+}
+
+fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const void* k, const void* v, const void* x,
+                         const void* w_f, const float* b_f, float* z, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  fox_status st = check_params(p);
+  if (st != FOX_OK) return st;
+  if (empty_problem(p)) return FOX_OK;
+  if (!q || !k || !v || !o || !lse) return FOX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = gate_proj(p, hidden, x, w_f, b_f, z, workspace, workspace_bytes, g, s);
+  if (st != FOX_OK) return st;
+  return fwd_after_gate(p, q, k, v, o, lse, workspace, g, s);
 }
 
 fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,

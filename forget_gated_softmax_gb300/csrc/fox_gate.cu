@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "fox_internal.h"
+#include "fox_ptx.cuh"
 
 namespace fox {
 namespace {
@@ -26,9 +27,43 @@ __device__ __forceinline__ float warp_inclusive_scan(float x, int lane) {
   return x;
 }
 
+// One warp scans one head's 128 tokens of tile T (4 per lane, serial, then a
+// shuffle scan) from column c of the staged log-gate values zs[token][c]
+// (log2 units, 0 past the sequence end), and writes the tile-local row terms,
+// the column record's 128 column terms and the tile total.
+__device__ __forceinline__ void scan_head_column(const float (*zs)[kHeadsPerPass + 1], int c, int lane, size_t bh,
+                                                 int T, int N, int nT, int Npad, int bias_from_j,
+                                                 float* __restrict__ rowloc, float* __restrict__ colrec,
+                                                 float* __restrict__ tiletot) {
+  const int t0 = T * kTile;
+  float a[4], incl[4];
+  float run = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    a[e] = zs[lane * 4 + e][c];
+    run += a[e];
+    incl[e] = run;
+  }
+  const float lane_incl = warp_inclusive_scan(run, lane);
+  const float excl_lane = lane_incl - run;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) incl[e] += excl_lane;
+  float4 rl = make_float4(incl[0], incl[1], incl[2], incl[3]);
+  *reinterpret_cast<float4*>(rowloc + bh * Npad + t0 + lane * 4) = rl;
+  float4 cl = bias_from_j ? make_float4(incl[0] - a[0], incl[1] - a[1], incl[2] - a[2], incl[3] - a[3]) : rl;
+  // keys past the sequence end get an infinite column term: x = ... - kappa = -inf, p = 0
+  const int tl = t0 + lane * 4;
+  if (tl + 0 >= N) cl.x = INFINITY;
+  if (tl + 1 >= N) cl.y = INFINITY;
+  if (tl + 2 >= N) cl.z = INFINITY;
+  if (tl + 3 >= N) cl.w = INFINITY;
+  *reinterpret_cast<float4*>(colrec + (bh * nT + T) * kColRec + lane * 4) = cl;
+  if (lane == 31) tiletot[bh * nT + T] = incl[3];
+}
+
 // One CTA per (tile T, batch b); all heads of that tile. z rows of one token
 // are contiguous over heads, so the load is coalesced; each warp then scans
-// one head's 128 tokens (4 per lane, serial, then a shuffle scan).
+// one head's 128 tokens.
 __global__ void __launch_bounds__(256) gate_tile_scan_kernel(const float* __restrict__ z, int B, int N, int H,
                                                              int nT, int Npad, int bias_from_j,
                                                              float* __restrict__ rowloc, float* __restrict__ colrec,
@@ -49,33 +84,160 @@ __global__ void __launch_bounds__(256) gate_tile_scan_kernel(const float* __rest
       zs[r][c] = a;
     }
     __syncthreads();
-    for (int c = warp; c < nh; c += blockDim.x / 32) {
-      const int h = h0 + c;
-      const size_t bh = (size_t)b * H + h;
-      float a[4], incl[4];
-      float run = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        a[e] = zs[lane * 4 + e][c];
-        run += a[e];
-        incl[e] = run;
-      }
-      const float lane_incl = warp_inclusive_scan(run, lane);
-      const float excl_lane = lane_incl - run;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) incl[e] += excl_lane;
-      float4 rl = make_float4(incl[0], incl[1], incl[2], incl[3]);
-      *reinterpret_cast<float4*>(rowloc + bh * Npad + t0 + lane * 4) = rl;
-      float4 cl = bias_from_j ? make_float4(incl[0] - a[0], incl[1] - a[1], incl[2] - a[2], incl[3] - a[3]) : rl;
-      // keys past the sequence end get an infinite column term: x = ... - kappa = -inf, p = 0
-      const int tl = t0 + lane * 4;
-      if (tl + 0 >= N) cl.x = INFINITY;
-      if (tl + 1 >= N) cl.y = INFINITY;
-      if (tl + 2 >= N) cl.z = INFINITY;
-      if (tl + 3 >= N) cl.w = INFINITY;
-      *reinterpret_cast<float4*>(colrec + (bh * nT + T) * kColRec + lane * 4) = cl;
-      if (lane == 31) tiletot[bh * nT + T] = incl[3];
+    for (int c = warp; c < nh; c += blockDim.x / 32)
+      scan_head_column(zs, c, lane, (size_t)b * H + h0 + c, T, N, nT, Npad, bias_from_j, rowloc, colrec, tiletot);
+  }
+}
+
+// ---------------------------------------------------------------- fused gate projection
+// z = x W_f^T + b_f ("Forgetting Transformer (FoX) Attention" module source:
+// f_proj = Linear(hidden_size, num_heads, bias=True), f = sigmoid(f_proj(x)))
+// fused with the tile scan above. CTA per (tile T, batch b): the tensor core
+// forms the 128 x H block of z for the tile's tokens (M = 128 tokens, N = H
+// padded to 16, K = hidden in chunks of 64 staged by TMA), and the epilogue
+// adds the bias, writes z, and scans it exactly as gate_tile_scan_kernel does.
+//   warp 0   TMA producer (x chunk 128 x 64, W chunk Hpad x 64; kProjStages stages)
+//   warp 1   TMEM allocator and MMA issuer
+//   warps 2-5 epilogue (thread = token = TMEM lane), then one head per warp in the scan
+constexpr int kProjThreads = 192;
+constexpr int kProjStages = 4;
+
+struct ProjParams {
+  int B, N, H, Hpad, hidden, nT, Npad, bias_from_j;
+  const float* bias;
+  float* z;  // [B, N, H] or null
+  float* rowloc;
+  float* colrec;
+  float* tiletot;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    gate_proj_scan_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                          const ProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t xb = kTile * 64 * 2;            // x chunk bytes (16 KB)
+  const uint32_t wb = (uint32_t)p.Hpad * 64 * 2;  // W chunk bytes (multiple of 2 KB)
+  uint8_t* sx = sm;
+  uint8_t* sw = sm + kProjStages * xb;
+  float(*zs)[kHeadsPerPass + 1] = reinterpret_cast<float(*)[kHeadsPerPass + 1]>(sw + kProjStages * wb);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kProjStages * wb + kTile * (kHeadsPerPass + 1) * 4);
+  // bars: FULL[kProjStages], EMPTY[kProjStages], DONE
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kProjStages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int T = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nK = (p.hidden + 63) / 64;
+  uint32_t tcols = 32;
+  while (tcols < (uint32_t)p.Hpad) tcols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kProjStages; ++s) {
+      mbar_init(&bars[s], 1);
+      mbar_init(&bars[kProjStages + s], 1);
     }
+    mbar_init(&bars[2 * kProjStages], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      tma_prefetch_desc(&tmap_w);
+      int issued = 0;
+      for (int kc = 0; kc < nK; ++kc) {
+        const int st = kc % kProjStages, n = kc / kProjStages;
+        if (n > 0 && !mbar_wait(&bars[kProjStages + st], (n - 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC))
+          break;
+        mbar_arrive_expect_tx(&bars[st], xb + wb);
+        tma_load_3d(sx + st * xb, &tmap_x, &bars[st], kc * 64, T * kTile, b);
+        tma_load_2d(sw + st * wb, &tmap_w, &bars[st], kc * 64, 0);
+        ++issued;
+      }
+      // every copy issued must land before shared memory is released
+      for (int kc = issued - kProjStages < 0 ? 0 : issued - kProjStages; kc < issued; ++kc)
+        mbar_wait_drain(&bars[kc % kProjStages], (kc / kProjStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTile, p.Hpad, false, false);
+      bool ok = true;
+      for (int kc = 0; kc < nK && ok; ++kc) {
+        const int st = kc % kProjStages;
+        ok = mbar_wait(&bars[st], (kc / kProjStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ax = smem_u32(sx + st * xb), aw = smem_u32(sw + st * wb);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_ss(tbase, sdesc_sw128(ax + ks * 32, 16, 1024), sdesc_sw128(aw + ks * 32, 16, 1024), idesc,
+                  (kc > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&bars[kProjStages + st]);
+      }
+      // DONE also follows the retirement of every MMA issued, so TMEM can be freed after it.
+      umma_commit(&bars[2 * kProjStages]);
+      if (!ok) mbar_wait_drain(&bars[2 * kProjStages], 0);
+    }
+    __syncwarp();
+  } else {
+    const int wq = warp & 3;  // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;
+    const int t = T * kTile + r;
+    const int ew = warp - 2;  // 0..3 within the epilogue warps
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    bool ok = mbar_wait(&bars[2 * kProjStages], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) && !*abort_flag;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) tc_fence_after();
+    for (int h0 = 0; h0 < p.H; h0 += kHeadsPerPass) {
+      const int nh = min(kHeadsPerPass, p.H - h0);
+      uint32_t acc[32];
+      if (ok) {
+        if (p.Hpad - h0 >= 32) {
+          tmem_ld32(tbase + lane_off + h0, acc);
+        } else {
+          tmem_ld16(tbase + lane_off + h0, acc);
+#pragma unroll
+          for (int c = 16; c < 32; ++c) acc[c] = 0u;
+        }
+        tmem_ld_wait();
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float a = 0.f;  // tokens past the end contribute log f = 0
+        if (ok && c < nh && t < p.N) {
+          const float zv = __uint_as_float(acc[c]) + p.bias[h0 + c];
+          if (p.z) p.z[((size_t)b * p.N + t) * p.H + h0 + c] = zv;
+          a = log_sigmoid(zv) * kLog2e;
+        }
+        zs[r][c] = a;
+      }
+      named_bar(1, 128);
+      if (ok)
+        for (int c = ew; c < nh; c += 4)
+          scan_head_column(zs, c, lane, (size_t)b * p.H + h0 + c, T, p.N, p.nT, p.Npad, p.bias_from_j, p.rowloc,
+                           p.colrec, p.tiletot);
+      named_bar(1, 128);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, tcols);
   }
 }
 
@@ -107,6 +269,50 @@ __global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, con
 }
 
 }  // namespace
+
+size_t gate_proj_smem_bytes(int H) {
+  const int Hpad = (H + 15) / 16 * 16;
+  return 1024 + kProjStages * (size_t)(kTile * 64 * 2 + Hpad * 64 * 2) + kTile * (kHeadsPerPass + 1) * 4 +
+         (2 * kProjStages + 1) * 8 + 16;
+}
+
+cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const float* bias, int hidden, float* z_out,
+                                  int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
+                                  cudaStream_t s) {
+  char* base = static_cast<char*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(base);
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);  // each call starts with a clean error word
+  if (e != cudaSuccess) return e;
+  ProjParams p;
+  p.B = B;
+  p.N = N;
+  p.H = H;
+  p.Hpad = (H + 15) / 16 * 16;
+  p.hidden = hidden;
+  p.nT = g.nT;
+  p.Npad = g.Npad;
+  p.bias_from_j = bias_from_j;
+  p.bias = bias;
+  p.z = z_out;
+  p.rowloc = reinterpret_cast<float*>(base + g.rowloc);
+  p.colrec = reinterpret_cast<float*>(base + g.colrec);
+  p.tiletot = reinterpret_cast<float*>(base + g.tiletot);
+  p.err = err;
+  const size_t smem = gate_proj_smem_bytes(H);
+  e = cudaFuncSetAttribute(gate_proj_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  {
+    TraceScope trace("gate_proj_scan", s);
+    gate_proj_scan_kernel<<<dim3(g.nT, B), kProjThreads, smem, s>>>(maps[0], maps[1], p);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    TraceScope trace("gate_base_scan", s);
+    gate_base_scan_kernel<<<(g.BH + 7) / 8, 256, 0, s>>>(g.BH, g.nT, p.tiletot, p.colrec);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
                              cudaStream_t s) {

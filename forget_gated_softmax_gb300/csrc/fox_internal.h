@@ -159,6 +159,13 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const Bwd
                             const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box) */,
                             cudaStream_t s);
 
+// Gate projection z = x W_f^T + b_f (tensor cores) fused with the tile scan, then the base
+// scan: fills the same gate terms as launch_gate_scan and writes z when z_out is set.
+// maps: x as [B, N, hidden] (box 64 x 128 x 1), W_f as [H, hidden] (box 64 x Hpad), both bf16,
+// 128-byte swizzle; H <= 256.
+cudaError_t launch_gate_proj_scan(const CUtensorMap* maps, const float* bias, int hidden, float* z_out, int B, int N,
+                                  int H, int bias_from_j, void* ws, const GateLayout& g, cudaStream_t s);
+
 // Decay-aware tile skipping: per-tile norms of q and k, then the key-tile span of every
 // query tile (jmin) and the query-tile span of every key tile (imax); needs the gate scan.
 cudaError_t launch_tile_span(const void* q, const void* k, int B, int N, int H, int d, float scale,
@@ -172,5 +179,9 @@ size_t window_workspace_bytes(int B, int N, int H);
 // box_rows tokens x 1 batch and 128-byte swizzle. Returns false when the driver entry point is
 // unavailable or encoding fails.
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows = kTile);
+// Host helpers for the gate projection: x [B, N, hidden] with a box of 64 x 128 x 1, and
+// W_f [H, hidden] with a box of 64 x (H rounded up to 16); bf16, 128-byte swizzle.
+bool make_x_map(CUtensorMap* map, const void* base, int B, int N, int hidden);
+bool make_wf_map(CUtensorMap* map, const void* base, int H, int hidden);
 
 }  // namespace fox

@@ -96,6 +96,31 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
                    float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Gate projection ("Forgetting Transformer (FoX) Attention" module source:
+ * f_proj = Linear(hidden_size, num_heads, bias=True), f = sigmoid(f_proj(x))):
+ *   z[b,t,h] = sum_e x[b,t,e] W_f[h,e] + b_f[h]
+ * x: [B,N,hidden] bf16. W_f: [H,hidden] bf16 (the Linear's weight layout).
+ * b_f: [H] fp32. z: [B,N,H] fp32. All arrays are device pointers.
+ * One kernel computes the 128-token x H blocks of z on the tensor cores
+ * (fp32 accumulation) and runs the gate scan of fox_fwd on them in the same
+ * pass, so fox_fwd_xgate's gate terms never round-trip through z.
+ * Requires dtype bf16, hidden a positive multiple of 8, and H <= 256.
+ * Workspace: fox_fwd_workspace_bytes(p) (its gate terms are also written).
+ */
+fox_status fox_gate_proj(const fox_params* p, int hidden, const void* x, const void* w_f, const float* b_f, float* z,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Forward from the layer input's gate projection instead of z: the fused
+ * projection + gate scan above, then the attention as in fox_fwd. Writes
+ * O, LSE and, when z is not null, z for the backward (fox_bwd takes z).
+ * The same requirements as fox_gate_proj apply; tile_skip is honoured.
+ */
+fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const void* k, const void* v, const void* x,
+                         const void* w_f, const float* b_f, float* z, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Backward (bf16 only). Reads q, k, v, z, the forward's O and LSE, and the
  * upstream gradient dO; writes dq, dk, dv [B,N,H,d] bf16 and dz [B,N,H] fp32.
  * Steps: gate scan, Delta_i = dO_i . O_i, the fused recompute-and-backward

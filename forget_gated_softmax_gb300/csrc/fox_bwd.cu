@@ -18,10 +18,9 @@
 //   bwd_main      one CTA per (b, h, 128-key tile J) over the query tiles I >= J
 //                 (all I when not causal), pipelined over 64-query half-tiles:
 //                 S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q and
-//                 dQ^T = K^T dS^T on the tensor core (tcgen05, TMEM), dQ reduced into
-//                 an fp32 accumulator; the column sums C_j stay in registers (the CTA
-//                 owns every column j of its tile) and the row sums R_i are reduced
-//                 across lanes and added into a global accumulator once per half-tile.
+//                 dQ^T = K^T dS^T on the tensor core (tcgen05, TMEM, two issuing warps),
+//                 dQ reduced into an fp32 accumulator; the row sums R_i and column sums
+//                 C_j of dS (added into global accumulators)
 //   bwd_dq        dQ = scale * accumulator -> bf16
 //   bwd_gate      reverse prefix scan of (R - C) and the sigmoid chain rule -> dz
 #include <cuda_bf16.h>
@@ -87,19 +86,28 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 
 // ------------------------------------------------------------------ main
 // One CTA per (b, h, 128-key tile J). The query tiles I >= J (every I when not
-// causal) are processed as half-tiles g = 0, 1, ... of 64 queries, software
-// pipelined over two tensor-memory buffers:
-//   MMA warp      S^T_g = K Q_g^T, dP^T_g = V dO_g^T into buffer g%2, then, once the
-//                 elementwise warps are done with g-1: dV += P^T_{g-1} dO_{g-1},
-//                 dK += dS^T_{g-1} Q_{g-1} and dQ^T_{g-1} = K^T dS^T_{g-1} (over the
-//                 freed buffer).
-//   8 elementwise P^T, dS^T of g (thread = key row x 32 queries) while the tensor
-//     warps        core runs g-1 / g+1; fp32 column sums C in registers, row sums R of g
-//                  by a shuffle reduce-scatter across the warp's 32 keys.
-//   4 readout     copy dQ^T_g out of tensor memory (buffer g%2 is handed back at once),
-//     warps       then reduce it into the fp32 dQ accumulator and R_g (the four lane
-//                 quarters' partials) into the row sums.
+// causal) are processed as half-tiles g = 0, 1, ... of 64 queries, pipelined
+// over two tensor-memory buffers x = g % 2 of 128 columns each:
+//   [0, 64)    S^T_g (fp32), then P^T_g packed bf16 in [0, 32) and dS^T_g in [32, 64)
+//   [64, 128)  dP^T_g (fp32), then dQ^T_g (fp32)
+// and the dK, dV accumulators in [256, 256 + 2D). Warp roles (480 threads):
+//   warp 13       S^T_g = K Q_g^T once dK / dV of g-2 have read P^T / dS^T out of the
+//                 buffer, dP^T_g = V dO_g^T once dQ^T_g-2 has been read out.
+//   warp 14       dV += P^T_g dO_g, dK += dS^T_g Q_g, then dQ^T_g = K^T dS^T_g (dS^T from
+//                 shared memory) once the elementwise warps are done with g.
+//                 (A single thread issues tcgen05.mma at a bounded rate, hence two.)
+//   8 elementwise P^T, dS^T of g (thread = key row x 32 queries); dS^T also goes to a
+//     warps        swizzled shared-memory buffer, the B operand of dQ^T.
+//   4 readout     the row sums R_g and column sums C of dS (see below), then copy dQ^T_g
+//     warps       out of tensor memory and reduce it into the fp32 dQ accumulator.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
+// The gate gradient needs R_i = sum_j dS_ij and C_j = sum_i dS_ij from the same
+// values (so that the suffix sums of R - C telescope over one matrix). Causal
+// (kExactSums = false): the readout warps sum the bf16 dS^T buffer in shared
+// memory, rows for C and columns for R, off the elementwise warps' path.
+// Non-causal (kExactSums = true): the gate gradient is a small difference of large
+// sums there, so the elementwise warps sum the fp32 values: C in registers, R by a
+// shuffle reduce-scatter across the warp's 32 keys.
 struct BwdKParams {
   int B, N, H, nT, Npad;
   int non_causal;
@@ -119,7 +127,7 @@ struct BwdKParams {
 
 constexpr int kHalf = 64;        // queries per half-tile
 constexpr int kStages = 3;       // Q / dO / Delta / rho stages
-constexpr int kBwdThreads = 448; // 14 warps
+constexpr int kBwdThreads = 480; // 15 warps
 
 template <int D>
 struct BwdLayoutSmem {
@@ -130,13 +138,14 @@ struct BwdLayoutSmem {
   static constexpr int kQ = 2 * kTileBytes;                    // kStages stages
   static constexpr int kDO = kQ + kStages * kHalfBytes;        // kStages stages
   static constexpr int kDS = kDO + kStages * kHalfBytes;       // 2 buffers of dS^T: 128 keys x 64 queries bf16
-  static constexpr int kZeros = kDS + 2 * 16384;               // 64-wide zero chunk (padding operand)
-  static constexpr int kDR = kZeros + 16384;                    // kStages x (Delta 256 B, rho 256 B)
+  static constexpr int kZeros = kDS + 2 * 16384;               // 64-wide zero chunk (padding operand, D = 64)
+  static constexpr int kZeroBytes = D == 64 ? 16384 : 0;
+  static constexpr int kDR = kZeros + kZeroBytes;              // kStages x (Delta 256 B, rho 256 B)
   static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
   static constexpr int kRsum = kRec + 1024;                    // [3 slots][4 lane quarters][64] row-sum partials
   static constexpr int kCs = kRsum + 3 * 4 * kHalf * 4;        // column-sum exchange, 128 floats
   static constexpr int kBars = kCs + 512;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 19;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
@@ -146,11 +155,13 @@ enum BwdBar {
   BB_KV = 0,
   BB_FULL = 1,    // +stage (3): Q, dO, Delta, rho of a half-tile landed
   BB_EMPTY = 4,   // +stage (3): the MMAs reading that stage retired
-  BB_SDP = 7,     // +buffer (2): S^T, dP^T in tensor memory
+  BB_SDP = 7,     // +buffer (2): S^T and dP^T in tensor memory
   BB_PDS = 9,     // +buffer (2): P^T, dS^T written (count 256)
-  BB_DQ = 11,     // +buffer (2): dQ^T and R in tensor memory; dS^T smem buffer free again
-  BB_DQFREE = 13, // +buffer (2): dQ^T read out, buffer free (count 128)
-  BB_FINAL = 15,  // last dK / dV MMAs retired
+  BB_DQ = 11,     // +buffer (2): dQ^T in tensor memory
+  BB_DQFREE = 13, // +buffer (2): dQ^T read out and the dS^T smem buffer summed (count 128)
+  BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
+  BB_BDONE = 16,  // every MMA of warp 13 retired
+  BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
 };
 
 // Barrier over `n` threads that also ORs a predicate across them: every thread gets the
@@ -173,20 +184,32 @@ __device__ __forceinline__ void red_add(float* p, float a) {
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+// The two bf16 halves of a packed word, as fp32: low half (even column), high half.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // P^T and dS^T for 32 queries of this thread's key row (columns c0 .. c0+31 of
 // the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
-// and [64+c0, 64+c0+32); packed bf16 P^T / dS^T go to [c0/2, c0/2+16) and
-// [64+c0/2, ...); the dS^T row piece goes to the swizzled smem buffer (queries
-// contiguous, MN-major). The row and column sums of dS are both formed on the
-// tensor core from these same bf16 values, so sum_s (R_s - C_s) over a suffix
-// sums one matrix and carries no rounding drift along the sequence.
-template <bool kDiag>
+// and [64+c0, 64+c0+32); packed bf16 P^T goes to [c0/2, c0/2+16) and dS^T to
+// [32+c0/2, 32+c0/2+16); the dS^T row piece goes to the swizzled smem buffer
+// (queries contiguous, MN-major). kExactSums: also the fp32 column sum (csum) and
+// this lane quarter's row-sum partials (rsum) of dS.
+template <bool kDiag, bool kExactSums>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
                                       const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp,
                                       float* rsum, float& csum) {
   uint32_t pp[16], dd[16];
-  float v[32];  // fp32 dS of this row's 32 queries, for the row and column sums
+  float v[32];  // fp32 dS of this row's 32 queries
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
     const float4 r4 = lds_f4(rh + c0 + 4 * e4);
@@ -201,7 +224,7 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
       if (kDiag && qoff + c0 + c < jr) x = -INFINITY;  // query before key: masked
       pv[e] = ex2_approx(x);
       v[c] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
-      csum += v[c];
+      if (kExactSums) csum += v[c];
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -209,29 +232,31 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     dd[2 * e4 + 1] = pack_bf16x2(v[4 * e4 + 2], v[4 * e4 + 3]);
   }
   tmem_st16(tX + (c0 >> 1), pp);
-  tmem_st16(tX + 64 + (c0 >> 1), dd);
+  tmem_st16(tX + 32 + (c0 >> 1), dd);
 #pragma unroll
   for (int pc = 0; pc < 4; ++pc) {
     const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
     sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
   }
-  // Row sums over this warp's 32 keys: reduce-scatter across the lanes (five halving
-  // rounds), after which lane l holds query c0 + l's sum.
-  const int lane = jr & 31;
+  if (kExactSums) {
+    // Row sums over this warp's 32 keys: reduce-scatter across the lanes (five halving
+    // rounds), after which lane l holds query c0 + l's sum.
+    const int lane = jr & 31;
 #pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
+    for (int half = 16; half >= 1; half >>= 1) {
+      const bool upper = (lane & half) != 0;
 #pragma unroll
-    for (int k = 0; k < half; ++k) {
-      const float send = upper ? v[k] : v[k + half];
-      const float keep = upper ? v[k + half] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+      for (int k = 0; k < half; ++k) {
+        const float send = upper ? v[k] : v[k + half];
+        const float keep = upper ? v[k + half] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+      }
     }
+    rsum[c0 + lane] = v[0];  // this lane quarter's partial; the readout adds the four quarters
   }
-  rsum[c0 + lane] = v[0];  // this lane quarter's partial; the readout adds the four quarters
 }
 
-template <int D>
+template <int D, bool kExactSums>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fox_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -269,8 +294,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars[BB_PDS + x], 256);
       mbar_init(&bars[BB_DQ + x], 1);
       mbar_init(&bars[BB_DQFREE + x], 128);
+      mbar_init(&bars[BB_KVD + x], 1);
     }
     mbar_init(&bars[BB_FINAL], 1);
+    mbar_init(&bars[BB_BDONE], 1);
     *abort_flag = 0;
     *G_shared = G;
     fence_mbar_init();
@@ -279,7 +306,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  {
+  if (D == 64) {
     // Constant operand: a 64-wide chunk of zeros, the upper M half of K^T when D = 64.
     uint32_t* zw = reinterpret_cast<uint32_t*>(sm + L::kZeros);
     for (int e = threadIdx.x; e < 16384 / 4; e += blockDim.x) zw[e] = 0u;
@@ -289,8 +316,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // Tensor memory: buffer x at [128x, 128x+128): S^T [0,64) | dP^T [64,128) (P^T packed over
-  // [0,32), dS^T over [64,96); dQ^T later over [0,64), R over [64,80)); dK [256, 256+D), dV after it.
 
   if (warp == 12) {
     // ------------------------------------------------------------- producer
@@ -328,96 +353,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (fills[st] > 0) mbar_wait_drain(&bars[BB_FULL + st], (fills[st] - 1) & 1);
     }
     __syncwarp();
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 13 || warp == 14) {
+    // ----------------------------------------------------------- MMA issuers
     if (lane == 0) {
       constexpr uint32_t hb = L::kHalfBytes;
       constexpr uint32_t idSP = idesc_bf16(128, kHalf, false, false);  // S^T, dP^T: M keys, N queries
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK: A from TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
-      const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
-      const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV), sQ = smem_u32(sm + L::kQ);
-      const uint32_t sdO = smem_u32(sm + L::kDO), sdS = smem_u32(sm + L::kDS);
-      const uint32_t sZeros = smem_u32(sm + L::kZeros);
-      // A = K^T: M = d channels (MN-major 64-wide chunks 16 KB apart; D = 64 pads the upper half with zeros)
-      const uint32_t kt_lbo = D == 128 ? 16384u : sZeros - sK;
-
-      auto batch = [&](int g) -> bool {  // dV, dK, dQ^T, R of half-tile g (buffer g & 1)
-        const int x = g & 1, st = g % kStages;
-        const uint32_t tX = tbase + 128 * x;
-        const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb, sdSx = sdS + x * 16384;
-        if (!mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kHalf / 16; ++ks)  // dV += P^T dO (K = 64 queries)
-          umma_ts(tdV, tX + ks * 8, sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
-          umma_ts(tdK, tX + 64 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [0,64)
-          umma_ss(tX, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024), idQ,
-                  ks > 0);
-        umma_commit(&bars[BB_DQ + x]);
-        umma_commit(&bars[BB_EMPTY + st]);
-        return true;
-      };
-
+      const uint32_t sK = smem_u32(sm + L::kK), sQ = smem_u32(sm + L::kQ), sdO = smem_u32(sm + L::kDO);
       bool ok = mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-      for (int g = 0; g < G && ok; ++g) {
-        const int x = g & 1, st = g % kStages;
-        const uint32_t tX = tbase + 128 * x;
-        const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb;
-        ok = mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-        if (ok && g >= 2) ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
-        if (!ok) break;
-        tc_fence_after();
+      if (warp == 13) {
+        const uint32_t sV = smem_u32(sm + L::kV);
+        for (int g = 0; g < G && ok; ++g) {
+          const int x = g & 1, st = g % kStages;
+          const uint32_t tX = tbase + 128 * x;
+          const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb;
+          ok = mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+          // S^T_g overwrites P^T / dS^T of g-2, read by warp 14's dV / dK of g-2
+          if (ok && g >= 2) ok = mbar_wait(&bars[BB_KVD + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;  // K / V tile: 128-row chunks
-          const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;   // Q / dO half-tile: 64-row chunks
-          umma_ss(tX, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQs + qoff, 16, 1024), idSP, ks > 0);
-        }
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;  // K / V tile: 128-row chunks
+            const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;   // Q / dO half-tile: 64-row chunks
+            umma_ss(tX, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQs + qoff, 16, 1024), idSP, ks > 0);
+          }
+          // dP^T_g overwrites dQ^T of g-2, which the readout warps must have copied out
+          if (g >= 2) ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-          const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;
-          umma_ss(tX + 64, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(sdOs + qoff, 16, 1024), idSP, ks > 0);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;
+            umma_ss(tX + 64, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(sdOs + qoff, 16, 1024), idSP, ks > 0);
+          }
+          umma_commit(&bars[BB_SDP + x]);
         }
-        umma_commit(&bars[BB_SDP + x]);
-        if (g >= 1) ok = batch(g - 1);
+      } else {
+        const uint32_t tdK = tbase + 256, tdV = tbase + 256 + D;
+        const uint32_t sdS = smem_u32(sm + L::kDS), sZeros = smem_u32(sm + L::kZeros);
+        // A = K^T: M = d channels (MN-major 64-wide chunks 16 KB apart; D = 64 pads the upper half with zeros)
+        const uint32_t kt_lbo = D == 128 ? 16384u : sZeros - sK;
+        for (int g = 0; g < G && ok; ++g) {
+          const int x = g & 1, st = g % kStages;
+          const uint32_t tX = tbase + 128 * x;
+          const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb, sdSx = sdS + x * 16384;
+          ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kHalf / 16; ++ks)  // dV += P^T dO (K = 64 queries)
+            umma_ts(tdV, tX + ks * 8, sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
+            umma_ts(tdK, tX + 32 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV,
+                    (g > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&bars[BB_KVD + x]);
+          umma_commit(&bars[BB_EMPTY + st]);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [64,128)
+            umma_ss(tX + 64, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024),
+                    idQ, ks > 0);
+          umma_commit(&bars[BB_DQ + x]);
+        }
       }
-      if (ok && G > 0) batch(G - 1);
-      umma_commit(&bars[BB_FINAL]);
-      mbar_wait_drain(&bars[BB_FINAL], 0);
+      // Every MMA this thread issued must retire before tensor memory is freed; for warp 14
+      // this is also the end of the dK / dV accumulation.
+      uint64_t* done = &bars[warp == 14 ? BB_FINAL : BB_BDONE];
+      umma_commit(done);
+      mbar_wait_drain(done, 0);
     }
     __syncwarp();
   } else if (warp >= 8) {
-    // ---------------------------------------------- dQ^T, R and C readout
+    // ------------------------------------------- R, C, dQ^T readout
     const int wq = warp & 3;
-    const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T, query of R, key of C
+    const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T; key row of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float* rpart = reinterpret_cast<float*>(sm + L::kRsum);  // [2][4][64] (causal) or [3][4][64] partials
+    float csum_r = 0.f;  // C_j of key j = ln (causal)
     bool ok = true;
     for (int g = 0; g < *G_shared && ok; ++g) {
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const int q0 = I_first * kTile + g * kHalf;
-      ok = mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
-           mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);  // row-sum partials
+      ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+      float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
+      if (!kExactSums && ok) {
+        const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
+        // C: the row of key ln (64 queries = 8 pieces of 16 B, swizzled by (piece ^ (row & 7)))
+        const uint32_t row = sdx + (uint32_t)ln * 128u;
+        float c_a = 0.f, c_b = 0.f;
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc) {
+          const uint4 w = lds_u4(row + (uint32_t)((pc ^ (ln & 7)) << 4));
+          c_a += (bf_lo(w.x) + bf_hi(w.x)) + (bf_lo(w.y) + bf_hi(w.y));
+          c_b += (bf_lo(w.z) + bf_hi(w.z)) + (bf_lo(w.w) + bf_hi(w.w));
+        }
+        csum_r += c_a + c_b;
+        // R: queries 2 lane and 2 lane + 1 (piece lane / 4, word lane % 4) over keys 32 wq .. 32 wq + 31
+        const uint32_t wofs = (uint32_t)(lane & 3) * 4u;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const int jr = wq * 32 + k;
+          const uint32_t w = lds_u32(sdx + (uint32_t)jr * 128u + (uint32_t)(((lane >> 2) ^ (jr & 7)) << 4) + wofs);
+          r_lo += bf_lo(w);
+          r_hi += bf_hi(w);
+        }
+        reinterpret_cast<float2*>(rpart + ((g & 1) * 4 + wq) * kHalf)[lane] = make_float2(r_lo, r_hi);
+      }
+      // The four readout warps meet once per half-tile (and agree whether to stop).
+      if (named_bar_any(6, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      if (!kExactSums && wq == 0) {  // R of the half-tile's 64 queries: the four key quarters
+        const float2* rp2 = reinterpret_cast<const float2*>(rpart + (g & 1) * 4 * kHalf);
+        const float2 a = rp2[lane], bq = rp2[kHalf / 2 + lane], c = rp2[kHalf + lane], d2 = rp2[3 * kHalf / 2 + lane];
+        atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane, (a.x + bq.x) + (c.x + d2.x));
+        atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane + 1, (a.y + bq.y) + (c.y + d2.y));
+      }
+      ok = mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t r0[32], r1[32], rv = 0;
-      tmem_ld32(tX + 0, r0);
-      tmem_ld32(tX + 32, r1);
+      tmem_ld32(tX + 64, r0);
+      tmem_ld32(tX + 96, r1);
       tmem_ld_wait();
-      if (wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
-        const float* rs = reinterpret_cast<const float*>(sm + L::kRsum) + (g % 3) * 4 * kHalf + ln;
+      if (kExactSums && wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
+        const float* rs = rpart + (g % 3) * 4 * kHalf + ln;
         rv = __float_as_uint((rs[0] + rs[kHalf]) + (rs[2 * kHalf] + rs[3 * kHalf]));
       }
       tc_fence_before();
-      mbar_arrive(&bars[BB_DQFREE + x]);  // the buffer's contents are in registers now
-      if (wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
+      mbar_arrive(&bars[BB_DQFREE + x]);  // dQ^T is in registers and the dS^T buffer has been summed
+      if (kExactSums && wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
       if (ln < D) {  // dQ[q0 + i][e] += dQ^T[e][i]: each reduction covers 32 consecutive floats of a row
         float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
 #pragma unroll
@@ -426,6 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i = 0; i < 32; ++i) red_add(dst + (size_t)(32 + i) * D, __uint_as_float(r1[i]));
       }
     }
+    if (!kExactSums && ok) p.colsum[(size_t)bh * p.Npad + J * kTile + ln] = csum_r;
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
     const int wq = warp & 3, ch = warp >> 2;
@@ -433,7 +505,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* rec = reinterpret_cast<const float*>(sm + L::kRec);
     const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
-    float csum = 0.f;  // C_j for key j = jr over this warp's queries of every half-tile
+    float csum = 0.f;  // kExactSums: C_j for key j = jr over this warp's queries of every half-tile
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
     ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
@@ -447,20 +519,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* rh = dlt + kHalf;
       float* rsum = reinterpret_cast<float*>(sm + L::kRsum) + ((g % 3) * 4 + wq) * kHalf;
       const float baseI_hi = recs[(size_t)I * kColRec + kTile], baseI_lo = recs[(size_t)I * kColRec + kTile + 1];
+      // SDP_g also orders this half-tile after the readout of g-2 (warp 13 waited for it
+      // before dP^T_g), which freed the dS^T smem buffer x.
       ok = mbar_wait(&bars[BB_SDP + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
            mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-      // dS^T smem buffer x is read by the dQ^T / R MMAs of half-tile g-2
-      if (ok && g >= 2) ok = mbar_wait(&bars[BB_DQ + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05 loads / stores below are warp-collective
       tc_fence_after();
       // x_ji (log2 units, minus the row offset) = scale2 * S^T_ji - kappa_j + (base_I - base_J) - rho_i
       const float cj = ((baseI_hi - baseJ_hi) + (baseI_lo - baseJ_lo)) - kap;
       const int c0 = ch * 32;
       const int qoff = half * kHalf;  // query offset of this half inside tile I (for the diagonal mask)
-      // Half ch = 1 overwrites packed columns [16, 32) and [80, 96), which hold S^T / dP^T of
-      // queries 16..31 read by ch = 0. Both warps of the lane quarter load, then meet on the
-      // quarter's barrier every iteration (so neither can run an iteration ahead), and the
-      // barrier's OR tells both whether either of them has to stop.
+      // Half ch = 1 writes P^T over columns [16, 32) (S^T of queries 16..31, read by ch = 0)
+      // and ch = 0 writes dS^T over [32, 48) (S^T of queries 32..47, read by ch = 1). Both warps
+      // of the lane quarter load, then meet on the quarter's barrier every iteration (so
+      // neither can run an iteration ahead), and the barrier's OR tells both whether either
+      // of them has to stop.
       uint32_t rs[32], rp[32];
       if (ok) {
         tmem_ld32(tX + c0, rs);
@@ -472,20 +545,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       if (causal && I == J)
-        pds32<true>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
+        pds32<true, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
       else
-        pds32<false>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
+        pds32<false, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BB_PDS + x]);
     }
-    // Column sums: half ch = 1 hands its partial to ch = 0 through shared memory.
-    float* cs = reinterpret_cast<float*>(sm + L::kCs);
-    if (ch == 1) cs[jr] = csum;
-    named_bar_any(5, 256, false);
     const int j = J * kTile + jr;
-    if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
+    if (kExactSums) {
+      // Column sums: half ch = 1 hands its partial to ch = 0 through shared memory.
+      float* cs = reinterpret_cast<float*>(sm + L::kCs);
+      if (ch == 1) cs[jr] = csum;
+      named_bar_any(5, 256, false);
+      if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
+    }
     // dK, dV epilogue
     if (ok) ok = mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
     ok = __all_sync(0xffffffffu, ok);
@@ -626,7 +701,8 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fox_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  auto kernel = a.non_causal ? fox_attn_bwd_kernel<D, true> : fox_attn_bwd_kernel<D, false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   BwdKParams p;
   p.B = a.B;
@@ -651,7 +727,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("attn_bwd", s);
-    fox_attn_bwd_kernel<D><<<(unsigned)blocks, kBwdThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], maps[3], p);
+    kernel<<<(unsigned)blocks, kBwdThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], maps[3], p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -98,16 +98,17 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 //                 (A single thread issues tcgen05.mma at a bounded rate, hence two.)
 //   8 elementwise P^T, dS^T of g (thread = key row x 32 queries); dS^T also goes to a
 //     warps        swizzled shared-memory buffer, the B operand of dQ^T.
-//   4 readout     the row sums R_g and column sums C of dS (see below), then copy dQ^T_g
-//     warps       out of tensor memory and reduce it into the fp32 dQ accumulator.
+//   4 readout     the row sums R_g of dS (see below), then copy dQ^T_g out of tensor
+//     warps       memory and reduce it into the fp32 dQ accumulator.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 // The gate gradient needs R_i = sum_j dS_ij and C_j = sum_i dS_ij from the same
 // values (so that the suffix sums of R - C telescope over one matrix). Causal
-// (kExactSums = false): the readout warps sum the bf16 dS^T buffer in shared
-// memory, rows for C and columns for R, off the elementwise warps' path.
-// Non-causal (kExactSums = true): the gate gradient is a small difference of large
-// sums there, so the elementwise warps sum the fp32 values: C in registers, R by a
-// shuffle reduce-scatter across the warp's 32 keys.
+// (kExactSums = false): both come from the bf16 dS values; the elementwise warps
+// keep C in registers and the readout warps sum the columns of the dS^T buffer in
+// shared memory for R, off the elementwise warps' path. Non-causal (kExactSums =
+// true): the gate gradient is a small difference of large sums there, so the
+// elementwise warps sum the fp32 values: C in registers, R by a shuffle
+// reduce-scatter across the warp's 32 keys.
 struct BwdKParams {
   int B, N, H, nT, Npad;
   int non_causal;
@@ -158,7 +159,7 @@ enum BwdBar {
   BB_SDP = 7,     // +buffer (2): S^T and dP^T in tensor memory
   BB_PDS = 9,     // +buffer (2): P^T, dS^T written (count 256)
   BB_DQ = 11,     // +buffer (2): dQ^T in tensor memory
-  BB_DQFREE = 13, // +buffer (2): dQ^T read out and the dS^T smem buffer summed (count 128)
+  BB_DQFREE = 13, // +buffer (2): dQ^T read out and the dS^T smem buffer's columns summed (count 128)
   BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
   BB_BDONE = 16,  // every MMA of warp 13 retired
   BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
@@ -184,11 +185,6 @@ __device__ __forceinline__ void red_add(float* p, float a) {
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -202,8 +198,9 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
 // and [64+c0, 64+c0+32); packed bf16 P^T goes to [c0/2, c0/2+16) and dS^T to
 // [32+c0/2, 32+c0/2+16); the dS^T row piece goes to the swizzled smem buffer
-// (queries contiguous, MN-major). kExactSums: also the fp32 column sum (csum) and
-// this lane quarter's row-sum partials (rsum) of dS.
+// (queries contiguous, MN-major). The column sum (csum) is accumulated from the
+// bf16 values, or from the fp32 ones with kExactSums, which also leaves this lane
+// quarter's row-sum partials in rsum.
 template <bool kDiag, bool kExactSums>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
                                       const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp,
@@ -230,6 +227,8 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
     dd[2 * e4] = pack_bf16x2(v[4 * e4], v[4 * e4 + 1]);
     dd[2 * e4 + 1] = pack_bf16x2(v[4 * e4 + 2], v[4 * e4 + 3]);
+    if (!kExactSums)  // the column sum of the bf16 values the readout's row sums also use
+      csum += (bf_lo(dd[2 * e4]) + bf_hi(dd[2 * e4])) + (bf_lo(dd[2 * e4 + 1]) + bf_hi(dd[2 * e4 + 1]));
   }
   tmem_st16(tX + (c0 >> 1), pp);
   tmem_st16(tX + 32 + (c0 >> 1), dd);
@@ -432,7 +431,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T; key row of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     float* rpart = reinterpret_cast<float*>(sm + L::kRsum);  // [2][4][64] (causal) or [3][4][64] partials
-    float csum_r = 0.f;  // C_j of key j = ln (causal)
     bool ok = true;
     for (int g = 0; g < *G_shared && ok; ++g) {
       const int x = g & 1;
@@ -442,16 +440,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
       if (!kExactSums && ok) {
         const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
-        // C: the row of key ln (64 queries = 8 pieces of 16 B, swizzled by (piece ^ (row & 7)))
-        const uint32_t row = sdx + (uint32_t)ln * 128u;
-        float c_a = 0.f, c_b = 0.f;
-#pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          const uint4 w = lds_u4(row + (uint32_t)((pc ^ (ln & 7)) << 4));
-          c_a += (bf_lo(w.x) + bf_hi(w.x)) + (bf_lo(w.y) + bf_hi(w.y));
-          c_b += (bf_lo(w.z) + bf_hi(w.z)) + (bf_lo(w.w) + bf_hi(w.w));
-        }
-        csum_r += c_a + c_b;
         // R: queries 2 lane and 2 lane + 1 (piece lane / 4, word lane % 4) over keys 32 wq .. 32 wq + 31
         const uint32_t wofs = (uint32_t)(lane & 3) * 4u;
 #pragma unroll 8
@@ -497,7 +485,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i = 0; i < 32; ++i) red_add(dst + (size_t)(32 + i) * D, __uint_as_float(r1[i]));
       }
     }
-    if (!kExactSums && ok) p.colsum[(size_t)bh * p.Npad + J * kTile + ln] = csum_r;
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
     const int wq = warp & 3, ch = warp >> 2;
@@ -505,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* rec = reinterpret_cast<const float*>(sm + L::kRec);
     const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
-    float csum = 0.f;  // kExactSums: C_j for key j = jr over this warp's queries of every half-tile
+    float csum = 0.f;  // C_j for key j = jr over this warp's queries of every half-tile
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
     ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
@@ -554,7 +541,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(&bars[BB_PDS + x]);
     }
     const int j = J * kTile + jr;
-    if (kExactSums) {
+    {
       // Column sums: half ch = 1 hands its partial to ch = 0 through shared memory.
       float* cs = reinterpret_cast<float*>(sm + L::kCs);
       if (ch == 1) cs[jr] = csum;

@@ -199,6 +199,43 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
   return s0 + s1;
 }
 
+// One pass over the row for the tiles after the first: p_j = 2^(t_j - off) into
+// registers (pk, packed bf16, not yet stored) together with max_j t_j (tmax), so
+// that S is read from tensor memory once. The caller stores pk over the first 64
+// columns, or, in the rare case that the row maximum grew past the threshold,
+// discards it and recomputes P with the new maximum (S is still intact then).
+__device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap, float scale2, float off,
+                                                   uint32_t* pk, float& tmax) {
+  float s0 = 0.f, s1 = 0.f, m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int qt = 0; qt < 4; ++qt) {
+    uint32_t raw[32];
+    tmem_ld32(tS + 32 * qt, raw);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const int j = 32 * qt + 4 * j4;
+      const float4 kk = lds_f4(kap + j);
+      float t[4];
+      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
+      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
+      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
+      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
+      m0 = fmaxf(m0, fmaxf(t[0], t[2]));
+      m1 = fmaxf(m1, fmaxf(t[1], t[3]));
+      float pr[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[e] = ex2_approx(t[e] - off);
+      s0 += pr[0] + pr[2];
+      s1 += pr[1] + pr[3];
+      pk[16 * qt + 2 * j4] = pack_bf16x2(pr[0], pr[1]);
+      pk[16 * qt + 2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
+    }
+  }
+  tmax = fmaxf(m0, m1);
+  return s0 + s1;
+}
+
 template <int D, bool kDelta>
 __global__ void __launch_bounds__(kThreads, 1)
     fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -432,21 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float* kap = reinterpret_cast<const float*>(sm + L::kKappa + st * kKappaBytes);
         const float beta = (baseI_hi - kap[kTile]) + (baseI_lo - kap[kTile + 1]);
-        // Cheap bound first; the exact row maximum only when the bound says the running
-        // maximum might be exceeded by more than the threshold (rare: the diagonal tile,
-        // visited first, holds the largest bias).
-        const float bound = row_bound(tS, p.scale2, kap[kTile - 1]) + beta;
-        float m_cand = bound;
-        bool grow = false;
-        if (__any_sync(0xffffffffu, bound > m_used + kRescaleThreshold)) {
-          m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
-          grow = m_cand > m_used + kRescaleThreshold;
-        }
-        if (__any_sync(0xffffffffu, grow)) {
-          // Some row's maximum grew by more than 2^8: rescale O and l of those rows
-          // (alpha = 1 for the others; the TMEM loads/stores are warp-collective, so
-          // the whole warp takes this branch). s_full of this tile was committed after
-          // the previous P V, so O is settled.
+        // Rescale O and l of the rows whose maximum grew by more than 2^8 (alpha = 1 for
+        // the others; the TMEM loads/stores are warp-collective, so the whole warp takes
+        // this branch). s_full of this tile was committed after the previous P V, so O is
+        // settled.
+        auto rescale = [&](float m_cand, bool grow) {
           const float alpha = grow ? ex2_approx(m_used - m_cand) : 1.f;
           l_sum *= alpha;
 #pragma unroll 1
@@ -459,8 +486,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c, o);
           }
           if (grow) m_used = m_cand;
+        };
+        if constexpr (kDelta) {
+          // Cheap bound first; the exact row maximum only when the bound says the running
+          // maximum might be exceeded by more than the threshold (rare: the first tile
+          // holds the largest bias).
+          const float bound = row_bound(tS, p.scale2, kap[kTile - 1]) + beta;
+          float m_cand = bound;
+          bool grow = false;
+          if (__any_sync(0xffffffffu, bound > m_used + kRescaleThreshold)) {
+            m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
+            grow = m_cand > m_used + kRescaleThreshold;
+          }
+          if (__any_sync(0xffffffffu, grow)) rescale(m_cand, grow);
+          l_sum += exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta, r);
+        } else {
+          // One pass with the running maximum; the exact row maximum comes with it.
+          uint32_t pk[64];
+          float tmax;
+          const float lsum_tile = exp_pass_deferred(tS, kap, p.scale2, m_used - beta, pk, tmax);
+          const float m_cand = tmax + beta;
+          const bool grow = m_cand > m_used + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, grow)) {  // rare: redo the tile with the new maximum
+            rescale(m_cand, grow);
+            l_sum += exp_pass<false, false>(tS, kap, p.scale2, m_used - beta, r);
+          } else {
+            l_sum += lsum_tile;
+            tmem_st32(tS, pk);
+            tmem_st32(tS + 32, pk + 32);
+          }
         }
-        l_sum += exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta, r);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_PFULL + k]);

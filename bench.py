@@ -492,6 +492,72 @@ def run_fox(args, rank: int, world: int, local_rank: int):
         dist.destroy_process_group()
 
 
+def run_configs(args):
+    """--configs: forward (and backward where the workload has one) of each named input
+    recipe on this GPU, CUDA-event timed; one JSON object per workload on stderr, and the
+    oracle's fp64 rate on the host for comparison. Not a bench line."""
+    import torch
+
+    import forget_gated_softmax_gb300 as fox
+
+    peaks, _ = measured_peaks()
+    stream = torch.cuda.current_stream()
+    for w in wl.ALL:
+        arrays = wl.draw(w)
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+        def dev(name):
+            a = arrays[name]
+            if name == "z" or w.dtype == "f32":
+                return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+            return torch.from_numpy(a.view(np.int16)).view(dt).cuda()
+
+        q, k, v, z = (dev(n) for n in ("q", "k", "v", "z"))
+        o, lse = torch.empty_like(q), torch.empty((w.B, w.N, w.H), dtype=torch.float32, device="cuda")
+        pf = fox.make_params(w.B, w.N, w.H, w.d, 0 if w.dtype == "bf16" else 1, 0.0, w.bias_from_j)
+        ws = fox.workspace(fox.fox_bwd_workspace_bytes(pf) if w.backward else fox.fox_fwd_workspace_bytes(pf), "cuda")
+        fwd = lambda: fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws, stream=stream)  # noqa: E731
+        res = {"workload": w.name, "dtype": w.dtype}
+        reps = 20
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fwd()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        res["fwd_ms"] = ms
+        res["fwd_tflops"] = w.fwd_flops() / (ms * 1e-3) / 1e12
+        if w.dtype == "bf16":
+            res["fwd_frac_of_burst_peak"] = res["fwd_tflops"] / peaks["bf16_tflops"]
+        if w.backward:
+            dO = dev("dO")
+            dq, dk, dv, dz = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(lse)
+            bwd = lambda: fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws,  # noqa: E731
+                                      stream=stream)
+            for _ in range(3):
+                bwd()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(reps):
+                bwd()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            res["bwd_ms"] = ms
+            res["bwd_tflops"] = w.bwd_flops() / (ms * 1e-3) / 1e12
+            res["bwd_frac_of_burst_peak"] = res["bwd_tflops"] / peaks["bf16_tflops"]
+        assert fox.fox_check_error(ws) == 0, "device-side error"
+        log(json.dumps(res))
+    if not args.no_cpu_baseline:
+        v_cpu, dt_cpu = oracle_sample(draw_inputs(WORKLOAD, 0, CPU_SAMPLE_TOKENS), CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+        log(json.dumps({"oracle": "fp64, all host cores", "tflops": v_cpu, "cores": blas_threads(),
+                        "sample": sample_desc(), "seconds": dt_cpu}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,6 +565,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("fox", "reference"), default="fox")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every named workload recipe (fwd, and bwd where it has one); results on stderr")
     ap.add_argument("--shape", default=None,
                     help="B,N,H,d of a smaller case of the same workload recipe (profiling runs; not a bench line)")
     args = ap.parse_args()
@@ -513,6 +581,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.configs:
+        run_configs(args)
         return
     run_fox(args, rank, world, local_rank)
 

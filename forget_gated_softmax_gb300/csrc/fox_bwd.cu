@@ -129,6 +129,7 @@ struct BwdKParams {
 constexpr int kHalf = 64;        // queries per half-tile
 constexpr int kStages = 3;       // Q / dO / Delta / rho stages
 constexpr int kBwdThreads = 480; // 15 warps
+constexpr int kHeadGroup = 8;    // heads whose key tiles are scheduled together
 
 template <int D>
 struct BwdLayoutSmem {
@@ -269,8 +270,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  const int J = static_cast<int>(blockIdx.x) / BH;  // key tile; J = 0 has the most query tiles
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // Work order: groups of kHeadGroup heads, and within a group the key tiles from J = 0
+  // (the most query tiles) down, the group's heads interleaved. The CTAs resident at
+  // once then share few heads, whose Q / dO streams stay in L2.
+  int J, bh;
+  {
+    const int idx = static_cast<int>(blockIdx.x);
+    const int full = (BH / kHeadGroup) * kHeadGroup * p.nT;  // CTAs in complete groups
+    const int gsize = idx < full ? kHeadGroup : BH % kHeadGroup;
+    const int gbase = idx < full ? (idx / (kHeadGroup * p.nT)) * kHeadGroup : BH - BH % kHeadGroup;
+    const int r = idx < full ? idx % (kHeadGroup * p.nT) : idx - full;
+    J = r / gsize;
+    bh = gbase + r % gsize;
+  }
   const int b = bh / p.H, h = bh % p.H;
   // Half-tiles of 64 queries: causal, query tiles I = J .. nT-1 (.. imax(J) with tile
   // skipping); non-causal, all of them.

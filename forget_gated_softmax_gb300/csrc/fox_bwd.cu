@@ -128,7 +128,7 @@ struct BwdKParams {
 
 constexpr int kHalf = 64;        // queries per half-tile
 constexpr int kStages = 3;       // Q / dO / Delta / rho stages
-constexpr int kBwdThreads = 480; // 15 warps
+constexpr int kBwdThreads = 512; // 16 warps = 4 warpgroups (warp 15 only donates registers)
 constexpr int kHeadGroup = 8;    // heads whose key tiles are scheduled together
 
 template <int D>
@@ -327,6 +327,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // Registers per warpgroup (launched at 128 each, 65536 in total): the producer and MMA
+  // warpgroup needs few, the readout warpgroup fewer than 128, and the elementwise
+  // warpgroups take the rest (256 x 144 + 128 x 112 + 128 x 112 = 65536).
+  // (The non-causal variant, with the fp32 row-sum shuffles in the elementwise warps,
+  // measured faster without the rebalancing.)
+  if (!kExactSums) {
+    if (warp >= 12)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+    else if (warp >= 8)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
+  }
 
   if (warp == 12) {
     // ------------------------------------------------------------- producer
@@ -437,6 +450,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(done, 0);
     }
     __syncwarp();
+  } else if (warp == 15) {
+    // no role
   } else if (warp >= 8) {
     // ------------------------------------------- R, C, dQ^T readout
     const int wq = warp & 3;

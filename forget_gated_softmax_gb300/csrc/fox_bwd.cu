@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 // over two tensor-memory buffers x = g % 2 of 128 columns each:
 //   [0, 64)    S^T_g (fp32), then P^T_g packed bf16 in [0, 32) and dS^T_g in [32, 64)
 //   [64, 128)  dP^T_g (fp32), then dQ^T_g (fp32)
-// and the dK, dV accumulators in [256, 256 + 2D). Warp roles (480 threads):
+// and the dK, dV accumulators in [256, 256 + 2D). Warp roles (512 threads; warp 15
+// has no role and in the causal variant gives its registers to the elementwise warps):
 //   warp 13       S^T_g = K Q_g^T once dK / dV of g-2 have read P^T / dS^T out of the
 //                 buffer, dP^T_g = V dO_g^T once dQ^T_g-2 has been read out.
 //   warp 14       dV += P^T_g dO_g, dK += dS^T_g Q_g, then dQ^T_g = K^T dS^T_g (dS^T from
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 //   4 readout     the row sums R_g of dS (see below), then copy dQ^T_g out of tensor
 //     warps       memory and reduce it into the fp32 dQ accumulator.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
+// CTAs are scheduled in groups of kHeadGroup heads (see the kernel).
 // The gate gradient needs R_i = sum_j dS_ij and C_j = sum_i dS_ij from the same
 // values (so that the suffix sums of R - C telescope over one matrix). Causal
 // (kExactSums = false): both come from the bf16 dS values; the elementwise warps

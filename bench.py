@@ -166,23 +166,32 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def sample_desc():
-    return (f"oracle forward+backward of heads (b=0, h=0..{CPU_SAMPLE_HEADS - 1}) of {WORKLOAD.name}, each cut to "
+def sample_desc(heads: int = CPU_SAMPLE_HEADS):
+    return (f"oracle forward+backward of heads (b=0, h=0..{heads - 1}) of {WORKLOAD.name}, each cut to "
             f"its first {CPU_SAMPLE_TOKENS} tokens (a causal prefix), fp64 numpy; TFLOP/s on nominal 7*N^2*d per head")
 
 
+REFERENCE_BUDGET_S = 120.0  # the whole --impl reference run (warm-up + timed steps) aims at about this
+
+
 def run_reference(args, rank: int):
+    """The oracle on the host cores: each step is forward + backward of a bounded sample of
+    the workload's heads (each cut to its first CPU_SAMPLE_TOKENS tokens), with the number of
+    heads per step chosen from a one-head calibration so that the run ends in a few minutes."""
     if rank != 0:
         return
     arrays = draw_inputs(WORKLOAD, rank, cut=CPU_SAMPLE_TOKENS)
+    _, t_head = oracle_sample(arrays, 1, CPU_SAMPLE_TOKENS)  # calibration, not counted
+    n_calls = max(1, args.steps + args.warmup)
+    heads = int(max(1, min(CPU_SAMPLE_HEADS, REFERENCE_BUDGET_S / (n_calls * max(t_head, 1e-3)))))
     for _ in range(args.warmup):
-        oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+        oracle_sample(arrays, heads, CPU_SAMPLE_TOKENS)
     vals, times = [], []
     for _ in range(args.steps):
-        v, dt = oracle_sample(arrays, CPU_SAMPLE_HEADS, CPU_SAMPLE_TOKENS)
+        v, dt = oracle_sample(arrays, heads, CPU_SAMPLE_TOKENS)
         vals.append(v)
         times.append(dt)
-    total_flops = args.steps * CPU_SAMPLE_HEADS * 7.0 * CPU_SAMPLE_TOKENS**2 * WORKLOAD.d
+    total_flops = args.steps * heads * 7.0 * CPU_SAMPLE_TOKENS**2 * WORKLOAD.d
     value = total_flops / sum(times) / 1e12
     cores = blas_threads()
     line = {
@@ -190,7 +199,8 @@ def run_reference(args, rank: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args.gpus),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample_desc()},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample_desc(heads)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -33,6 +33,14 @@ namespace fox {
 namespace {
 
 
+// The fp32 dQ accumulator is blocked so that the 32 queries x 32 channels that one readout
+// warp adds at a time form one contiguous 4 KB block: [bh][Npad / 32][D / 32][32][32].
+template <int D>
+__device__ __forceinline__ size_t dq_offset(size_t bh, int Npad, int i, int e) {
+  return ((((bh * (size_t)(Npad >> 5) + (size_t)(i >> 5)) * (D / 32) + (size_t)(e >> 5)) << 10) +
+         (size_t)((i & 31) << 5) + (size_t)(e & 31));
+}
+
 // ------------------------------------------------------------------ rows
 // One warp per (b, i, h) with i in [0, Npad).
 template <int D>
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  float* dq = dqacc + (bh * Npad + i) * D + lane * E;
+  float* dq = dqacc + dq_offset<D>(bh, Npad, i, lane * E);
 #pragma unroll
   for (int e = 0; e < E; ++e) dq[e] = 0.f;
   if (lane == 0) {
@@ -88,7 +96,8 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 // One CTA per (b, h, 128-key tile J). The query tiles I >= J (every I when not
 // causal) are processed as half-tiles g = 0, 1, ... of 64 queries, pipelined
 // over two tensor-memory buffers x = g % 2 of 128 columns each:
-//   [0, 64)    S^T_g (fp32), then P^T_g packed bf16 in [0, 32) and dS^T_g in [32, 64)
+//   [0, 64)    S^T_g (fp32), then P^T_g and dS^T_g packed bf16: queries 32h .. 32h + 31
+//              (h = 0, 1) of P^T in [32h, 32h + 16), of dS^T in [32h + 16, 32h + 32)
 //   [64, 128)  dP^T_g (fp32), then dQ^T_g (fp32)
 // and the dK, dV accumulators in [256, 256 + 2D). Warp roles (512 threads; warp 15
 // has no role and in the causal variant gives its registers to the elementwise warps):
@@ -129,6 +138,9 @@ struct BwdKParams {
 };
 
 constexpr int kHalf = 64;        // queries per half-tile
+// First tensor-memory column of K step ks (16 queries, 8 packed columns) of P^T in a buffer;
+// dS^T's is 16 columns further. Queries 32h .. 32h + 31 sit in [32h, 32h + 32).
+__host__ __device__ constexpr uint32_t pds_col(int ks) { return (uint32_t)((ks >> 1) * 32 + (ks & 1) * 8); }
 constexpr int kStages = 3;       // Q / dO / Delta / rho stages
 constexpr int kBwdThreads = 512; // 16 warps = 4 warpgroups (warp 15 only donates registers)
 constexpr int kHeadGroup = 8;    // heads whose key tiles are scheduled together
@@ -144,12 +156,13 @@ struct BwdLayoutSmem {
   static constexpr int kDS = kDO + kStages * kHalfBytes;       // 2 buffers of dS^T: 128 keys x 64 queries bf16
   static constexpr int kZeros = kDS + 2 * 16384;               // 64-wide zero chunk (padding operand, D = 64)
   static constexpr int kZeroBytes = D == 64 ? 16384 : 0;
-  static constexpr int kDR = kZeros + kZeroBytes;              // kStages x (Delta 256 B, rho 256 B)
+  static constexpr int kDQ = kZeros + kZeroBytes;              // dQ staging: 4 readout warps x 4 KB
+  static constexpr int kDR = kDQ + 16384;                      // kStages x (Delta 256 B, rho 256 B)
   static constexpr int kRec = kDR + kStages * 512;             // column record of tile J (528 B)
   static constexpr int kRsum = kRec + 1024;                    // [3 slots][4 lane quarters][64] row-sum partials
   static constexpr int kCs = kRsum + 3 * 4 * kHalf * 4;        // column-sum exchange, 128 floats
   static constexpr int kBars = kCs + 512;
-  static constexpr int kNumBars = 19;
+  static constexpr int kNumBars = 21;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
@@ -166,6 +179,7 @@ enum BwdBar {
   BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
   BB_BDONE = 16,  // every MMA of warp 13 retired
   BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
+  BB_DSFREE = 19, // +buffer (2): dQ staged over the dS^T smem buffer has been read out (count 4)
 };
 
 // Barrier over `n` threads that also ORs a predicate across them: every thread gets the
@@ -182,8 +196,8 @@ __device__ __forceinline__ bool named_bar_any(int id, int n, bool pred) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void red_add(float* p, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+__device__ __forceinline__ void sts_f32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -199,16 +213,16 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 // P^T and dS^T for 32 queries of this thread's key row (columns c0 .. c0+31 of
 // the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
-// and [64+c0, 64+c0+32); packed bf16 P^T goes to [c0/2, c0/2+16) and dS^T to
-// [32+c0/2, 32+c0/2+16); the dS^T row piece goes to the swizzled smem buffer
-// (queries contiguous, MN-major). The column sum (csum) is accumulated from the
+// and [64+c0, 64+c0+32); packed bf16 P^T goes to [c0, c0+16) and dS^T to
+// [c0+16, c0+32) (over the S^T values just loaded), and the packed dS^T words are left in dd for the caller to
+// store into the swizzled smem buffer. The column sum (csum) is accumulated from the
 // bf16 values, or from the fp32 ones with kExactSums, which also leaves this lane
 // quarter's row-sum partials in rsum.
 template <bool kDiag, bool kExactSums>
 __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, float scale2, float cj, const float* dlt,
-                                      const float* rh, uint32_t sds_row, const uint32_t* rs, const uint32_t* rp,
-                                      float* rsum, float& csum) {
-  uint32_t pp[16], dd[16];
+                                      const float* rh, const uint32_t* rs, const uint32_t* rp, float* rsum,
+                                      float& csum, uint32_t* dd) {
+  uint32_t pp[16];
   float v[32];  // fp32 dS of this row's 32 queries
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
@@ -233,13 +247,8 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     if (!kExactSums)  // the column sum of the bf16 values the readout's row sums also use
       csum += (bf_lo(dd[2 * e4]) + bf_hi(dd[2 * e4])) + (bf_lo(dd[2 * e4 + 1]) + bf_hi(dd[2 * e4 + 1]));
   }
-  tmem_st16(tX + (c0 >> 1), pp);
-  tmem_st16(tX + 32 + (c0 >> 1), dd);
-#pragma unroll
-  for (int pc = 0; pc < 4; ++pc) {
-    const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
-    sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2], dd[4 * pc + 3]);
-  }
+  tmem_st16(tX + c0, pp);
+  tmem_st16(tX + c0 + 16, dd);
   if (kExactSums) {
     // Row sums over this warp's 32 keys: reduce-scatter across the lanes (five halving
     // rounds), after which lane l holds query c0 + l's sum.
@@ -308,6 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars[BB_DQ + x], 1);
       mbar_init(&bars[BB_DQFREE + x], 128);
       mbar_init(&bars[BB_KVD + x], 1);
+      mbar_init(&bars[BB_DSFREE + x], 4);
     }
     mbar_init(&bars[BB_FINAL], 1);
     mbar_init(&bars[BB_BDONE], 1);
@@ -431,10 +441,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kHalf / 16; ++ks)  // dV += P^T dO (K = 64 queries)
-            umma_ts(tdV, tX + ks * 8, sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+            umma_ts(tdV, tX + pds_col(ks), sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
-            umma_ts(tdK, tX + 32 + ks * 8, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV,
+            umma_ts(tdK, tX + pds_col(ks) + 16, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV,
                     (g > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bars[BB_KVD + x]);
           umma_commit(&bars[BB_EMPTY + st]);
@@ -460,12 +470,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int ln = wq * 32 + lane;  // TMEM lane: output channel of dQ^T; key row of C
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     float* rpart = reinterpret_cast<float*>(sm + L::kRsum);  // [2][4][64] (causal) or [3][4][64] partials
-    bool ok = true;
+    const uint32_t stage = smem_u32(sm + L::kDQ) + (uint32_t)wq * 4096u;
+    float* dq_bh = p.dqacc + (size_t)bh * p.Npad * D;  // this (b, h)'s slab of the blocked accumulator
+    bool ok = true, staged = false;
     for (int g = 0; g < *G_shared && ok; ++g) {
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const int q0 = I_first * kTile + g * kHalf;
       ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+      // The first dQ block of g - 1 went over the dS^T buffer of g - 1. Once the bulk engine
+      // has read it (by now it normally has), the elementwise warps may write that buffer for
+      // g + 1. (Waiting for the read right after issuing it stalled them.)
+      if (staged && lane == 0) {
+        bulk_wait_read<1>();
+        mbar_arrive(&bars[BB_DSFREE + (x ^ 1)]);
+      }
+      staged = false;
       float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
       if (!kExactSums && ok) {
         const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
@@ -506,14 +526,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[BB_DQFREE + x]);  // dQ^T is in registers and the dS^T buffer has been summed
       if (kExactSums && wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
-      if (ln < D) {  // dQ[q0 + i][e] += dQ^T[e][i]: each reduction covers 32 consecutive floats of a row
-        float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
+      if (wq * 32 < D) {
+        // dQ[q0 + i][32 wq + lane] += dQ^T[32 wq + lane][i], as two blocks of 32 queries x 32
+        // channels staged in shared memory and added into the accumulator by the bulk-copy
+        // engine. The first block goes over this warp's own rows of the dS^T buffer x (the
+        // dQ^T MMA and this warp's row sums are done with them), the second into the warp's
+        // staging block once the block staged there for g - 1 has been read.
+        const uint32_t stage_a = smem_u32(sm + L::kDS + x * 16384) + (uint32_t)wq * 4096u;
+        float* blk = dq_bh + ((size_t)(q0 >> 5) * (D / 32) + wq) * 1024;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) red_add(dst + (size_t)i * D, __uint_as_float(r0[i]));
+        for (int i = 0; i < 32; ++i) sts_f32(stage_a + (uint32_t)(i * 32 + lane) * 4u, r0[i]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_reduce_add_f32(blk, stage_a, 4096);
+          bulk_commit_group();
+          bulk_wait_read<1>();
+        }
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) red_add(dst + (size_t)(32 + i) * D, __uint_as_float(r1[i]));
+        for (int i = 0; i < 32; ++i) sts_f32(stage + (uint32_t)(i * 32 + lane) * 4u, r1[i]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_reduce_add_f32(blk + (D / 32) * 1024, stage, 4096);
+          bulk_commit_group();
+        }
       }
+      staged = true;
     }
+    if (lane == 0) bulk_wait_all();  // every reduction has landed in the accumulator
+    __syncwarp();
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
     const int wq = warp & 3, ch = warp >> 2;
@@ -523,7 +566,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float* recs = p.colrec + (size_t)bh * p.nT * kColRec;
     float csum = 0.f;  // C_j for key j = jr over this warp's queries of every half-tile
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA));
-    ok = !named_bar_any(1 + wq, 64, !ok);  // both warps of the lane quarter enter the loop, or neither
     const float kap = ok ? rec[jr] : 0.f;
     const float baseJ_hi = ok ? rec[kTile] : 0.f, baseJ_lo = ok ? rec[kTile + 1] : 0.f;
     for (int g = 0; g < *G_shared && ok; ++g) {
@@ -545,25 +587,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float cj = ((baseI_hi - baseJ_hi) + (baseI_lo - baseJ_lo)) - kap;
       const int c0 = ch * 32;
       const int qoff = half * kHalf;  // query offset of this half inside tile I (for the diagonal mask)
-      // Half ch = 1 writes P^T over columns [16, 32) (S^T of queries 16..31, read by ch = 0)
-      // and ch = 0 writes dS^T over [32, 48) (S^T of queries 32..47, read by ch = 1). Both warps
-      // of the lane quarter load, then meet on the quarter's barrier every iteration (so
-      // neither can run an iteration ahead), and the barrier's OR tells both whether either
-      // of them has to stop.
+      // Each warp packs P^T and dS^T of its 32 queries over the S^T columns it has just
+      // loaded ([c0, c0 + 32)), so the two warps of a lane quarter never touch each other's
+      // columns and need no barrier between them.
+      if (!ok) break;
       uint32_t rs[32], rp[32];
-      if (ok) {
-        tmem_ld32(tX + c0, rs);
-        tmem_ld32(tX + 64 + c0, rp);
-        tmem_ld_wait();
-      }
-      if (named_bar_any(1 + wq, 64, !ok)) {
-        ok = false;
-        break;
-      }
+      tmem_ld32(tX + c0, rs);
+      tmem_ld32(tX + 64 + c0, rp);
+      tmem_ld_wait();
+      uint32_t dd[16];
       if (causal && I == J)
-        pds32<true, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
+        pds32<true, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, rs, rp, rsum, csum, dd);
       else
-        pds32<false, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, sds_row, rs, rp, rsum, csum);
+        pds32<false, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, rs, rp, rsum, csum, dd);
+      // The readout staged dQ of g - 2 over this dS^T buffer; the bulk engine must have read it.
+      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars[BB_DSFREE + x], ((g - 2) >> 1) & 1, abort_flag,
+                                                       p.err, DEV_ERR_TIMEOUT_SYNC)))
+        break;
+#pragma unroll
+      for (int pc = 0; pc < 4; ++pc) {
+        const int piece = (c0 >> 3) + pc;  // 16-byte piece = 8 queries
+        sts_v4(sds_row + (uint32_t)((piece ^ (jr & 7)) << 4), dd[4 * pc], dd[4 * pc + 1], dd[4 * pc + 2],
+               dd[4 * pc + 3]);
+      }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -632,7 +678,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Np
   const long long bi = row / H;
   const int i = (int)(bi % N);
   const int b = (int)(bi / N);
-  const float* src = dqacc + (((size_t)b * H + h) * Npad + i) * D + lane * E;
+  const float* src = dqacc + dq_offset<D>((size_t)b * H + h, Npad, i, lane * E);
   __nv_bfloat16* dst = dq + (size_t)row * D + lane * E;
   if (E == 4) {
     const float4 v = *reinterpret_cast<const float4*>(src);

@@ -207,9 +207,18 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-// The two bf16 halves of a packed word, as fp32: low half (even column), high half.
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// c + the low (even column) or high bf16 half of a packed word, widened exactly to fp32
+// (one mixed-precision add: the same result as widening first and adding in fp32).
+__device__ __forceinline__ float add_bf_lo(float c, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, %2;\n\t}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_bf_hi(float c, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, %2;\n\t}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
 
 // P^T and dS^T for 32 queries of this thread's key row (columns c0 .. c0+31 of
 // the half-tile). S^T / dP^T values come from tensor memory columns [c0, c0+32)
@@ -232,20 +241,31 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
     const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
     float pv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4; e += 2) {  // element pairs in packed fp32
       const int c = 4 * e4 + e;
-      float x = fmaf(__uint_as_float(rs[c]), scale2, cj) - rr[e];
-      if (kDiag && qoff + c0 + c < jr) x = -INFINITY;  // query before key: masked
-      pv[e] = ex2_approx(x);
-      v[c] = pv[e] * (__uint_as_float(rp[c]) - dl[e]);
-      if (kExactSums) csum += v[c];
+      float2 x = fsub2(ffma2(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
+                             make_float2(scale2, scale2), make_float2(cj, cj)),
+                       make_float2(rr[e], rr[e + 1]));
+      if (kDiag && qoff + c0 + c < jr) x.x = -INFINITY;  // query before key: masked
+      if (kDiag && qoff + c0 + c + 1 < jr) x.y = -INFINITY;
+      pv[e] = ex2_approx(x.x);
+      pv[e + 1] = ex2_approx(x.y);
+      const float2 t = fmul2(make_float2(pv[e], pv[e + 1]),
+                             fsub2(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
+                                   make_float2(dl[e], dl[e + 1])));
+      v[c] = t.x;
+      v[c + 1] = t.y;
+      if (kExactSums) {
+        csum += v[c];
+        csum += v[c + 1];
+      }
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
     dd[2 * e4] = pack_bf16x2(v[4 * e4], v[4 * e4 + 1]);
     dd[2 * e4 + 1] = pack_bf16x2(v[4 * e4 + 2], v[4 * e4 + 3]);
     if (!kExactSums)  // the column sum of the bf16 values the readout's row sums also use
-      csum += (bf_lo(dd[2 * e4]) + bf_hi(dd[2 * e4])) + (bf_lo(dd[2 * e4 + 1]) + bf_hi(dd[2 * e4 + 1]));
+      csum = add_bf_hi(add_bf_lo(add_bf_hi(add_bf_lo(csum, dd[2 * e4]), dd[2 * e4]), dd[2 * e4 + 1]), dd[2 * e4 + 1]);
   }
   tmem_st16(tX + c0, pp);
   tmem_st16(tX + c0 + 16, dd);
@@ -495,8 +515,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int k = 0; k < 32; ++k) {
           const int jr = wq * 32 + k;
           const uint32_t w = lds_u32(sdx + (uint32_t)jr * 128u + (uint32_t)(((lane >> 2) ^ (jr & 7)) << 4) + wofs);
-          r_lo += bf_lo(w);
-          r_hi += bf_hi(w);
+          r_lo = add_bf_lo(r_lo, w);
+          r_hi = add_bf_hi(r_hi, w);
         }
         reinterpret_cast<float2*>(rpart + ((g & 1) * 4 + wq) * kHalf)[lane] = make_float2(r_lo, r_hi);
       }

@@ -94,9 +94,13 @@ enum Bar {
 
 // Row maximum of t_j = scale2 * S_j - kappa_j over the 128 columns of this
 // thread's S row in tensor memory (columns j > r masked on the diagonal tile).
+// The loops below work on column pairs in packed fp32 with the negated argument
+// tn_j = kappa_j - scale2 * S_j = -t_j (exactly, as rounding is symmetric), so that the
+// column term enters without a negation; t_j - off is then (-off) - tn_j, again exact.
 template <bool kDiag>
 __device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float scale2, int r) {
-  float m0 = -INFINITY, m1 = -INFINITY;
+  const float2 nsc = make_float2(-scale2, -scale2);
+  float mn = INFINITY;  // min_j tn_j
 #pragma unroll
   for (int qt = 0; qt < 4; ++qt) {
     uint32_t raw[32];
@@ -106,21 +110,20 @@ __device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float sc
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;
       const float4 kk = lds_f4(kap + j);
-      float t[4];
-      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
-      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
-      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
-      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
+      float2 a = ffma2(make_float2(__uint_as_float(raw[4 * j4]), __uint_as_float(raw[4 * j4 + 1])), nsc,
+                       make_float2(kk.x, kk.y));
+      float2 c = ffma2(make_float2(__uint_as_float(raw[4 * j4 + 2]), __uint_as_float(raw[4 * j4 + 3])), nsc,
+                       make_float2(kk.z, kk.w));
       if (kDiag) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (j + e > r) t[e] = -INFINITY;
+        if (j > r) a.x = INFINITY;
+        if (j + 1 > r) a.y = INFINITY;
+        if (j + 2 > r) c.x = INFINITY;
+        if (j + 3 > r) c.y = INFINITY;
       }
-      m0 = fmaxf(m0, fmaxf(t[0], t[2]));
-      m1 = fmaxf(m1, fmaxf(t[1], t[3]));
+      mn = fmin3(fmin3(mn, a.x, a.y), c.x, c.y);
     }
   }
-  return fmaxf(m0, m1);
+  return -mn;
 }
 
 // Upper bound of this row's t_j = scale2 * S_j - kappa_j over a tile without
@@ -152,7 +155,8 @@ __device__ __forceinline__ float row_bound(uint32_t tS, float scale2, float kapp
 // [32q+16, 32q+32), the chunk's own columns, and both feed the P V product.
 template <bool kDiag, bool kSplit = false>
 __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float scale2, float off, int r) {
-  float s0 = 0.f, s1 = 0.f;
+  const float2 nsc = make_float2(-scale2, -scale2), noff = make_float2(-off, -off);
+  float2 s = make_float2(0.f, 0.f);  // sums of the even and odd columns
 #pragma unroll
   for (int qt = 0; qt < 4; ++qt) {
     uint32_t raw[32];
@@ -164,21 +168,23 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;
       const float4 kk = lds_f4(kap + j);
-      float t[4];
-      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
-      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
-      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
-      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
+      // w = t - off for columns j .. j+3
+      float2 wa = fsub2(noff, ffma2(make_float2(__uint_as_float(raw[4 * j4]), __uint_as_float(raw[4 * j4 + 1])),
+                                    nsc, make_float2(kk.x, kk.y)));
+      float2 wc = fsub2(noff, ffma2(make_float2(__uint_as_float(raw[4 * j4 + 2]), __uint_as_float(raw[4 * j4 + 3])),
+                                    nsc, make_float2(kk.z, kk.w)));
       if (kDiag) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (j + e > r) t[e] = -INFINITY;
+        if (j > r) wa.x = -INFINITY;
+        if (j + 1 > r) wa.y = -INFINITY;
+        if (j + 2 > r) wc.x = -INFINITY;
+        if (j + 3 > r) wc.y = -INFINITY;
       }
       float pr[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pr[e] = ex2_approx(t[e] - off);
-      s0 += pr[0] + pr[2];
-      s1 += pr[1] + pr[3];
+      pr[0] = ex2_approx(wa.x);
+      pr[1] = ex2_approx(wa.y);
+      pr[2] = ex2_approx(wc.x);
+      pr[3] = ex2_approx(wc.y);
+      s = fadd2(s, fadd2(make_float2(pr[0], pr[1]), make_float2(pr[2], pr[3])));
       pk[2 * j4] = pack_bf16x2(pr[0], pr[1]);
       pk[2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
       if (kSplit) {
@@ -196,7 +202,7 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
       tmem_st16(tS + 16 * qt, pk);
     }
   }
-  return s0 + s1;
+  return s.x + s.y;
 }
 
 // One pass over the row for the tiles after the first: p_j = 2^(t_j - off) into
@@ -206,7 +212,9 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
 // discards it and recomputes P with the new maximum (S is still intact then).
 __device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap, float scale2, float off,
                                                    uint32_t* pk, float& tmax) {
-  float s0 = 0.f, s1 = 0.f, m0 = -INFINITY, m1 = -INFINITY;
+  const float2 nsc = make_float2(-scale2, -scale2), noff = make_float2(-off, -off);
+  float2 s = make_float2(0.f, 0.f);  // sums of the even and odd columns
+  float mn = INFINITY;                // min_j tn_j = -max_j t_j
 #pragma unroll
   for (int qt = 0; qt < 4; ++qt) {
     uint32_t raw[32];
@@ -216,24 +224,24 @@ __device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;
       const float4 kk = lds_f4(kap + j);
-      float t[4];
-      t[0] = fmaf(__uint_as_float(raw[4 * j4 + 0]), scale2, -kk.x);
-      t[1] = fmaf(__uint_as_float(raw[4 * j4 + 1]), scale2, -kk.y);
-      t[2] = fmaf(__uint_as_float(raw[4 * j4 + 2]), scale2, -kk.z);
-      t[3] = fmaf(__uint_as_float(raw[4 * j4 + 3]), scale2, -kk.w);
-      m0 = fmaxf(m0, fmaxf(t[0], t[2]));
-      m1 = fmaxf(m1, fmaxf(t[1], t[3]));
+      const float2 a = ffma2(make_float2(__uint_as_float(raw[4 * j4]), __uint_as_float(raw[4 * j4 + 1])), nsc,
+                             make_float2(kk.x, kk.y));
+      const float2 c = ffma2(make_float2(__uint_as_float(raw[4 * j4 + 2]), __uint_as_float(raw[4 * j4 + 3])), nsc,
+                             make_float2(kk.z, kk.w));
+      mn = fmin3(fmin3(mn, a.x, a.y), c.x, c.y);
+      const float2 wa = fsub2(noff, a), wc = fsub2(noff, c);  // t - off
       float pr[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pr[e] = ex2_approx(t[e] - off);
-      s0 += pr[0] + pr[2];
-      s1 += pr[1] + pr[3];
+      pr[0] = ex2_approx(wa.x);
+      pr[1] = ex2_approx(wa.y);
+      pr[2] = ex2_approx(wc.x);
+      pr[3] = ex2_approx(wc.y);
+      s = fadd2(s, fadd2(make_float2(pr[0], pr[1]), make_float2(pr[2], pr[3])));
       pk[16 * qt + 2 * j4] = pack_bf16x2(pr[0], pr[1]);
       pk[16 * qt + 2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
     }
   }
-  tmax = fmaxf(m0, m1);
-  return s0 + s1;
+  tmax = -mn;
+  return s.x + s.y;
 }
 
 template <int D, bool kDelta>

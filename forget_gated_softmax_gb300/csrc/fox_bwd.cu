@@ -175,11 +175,12 @@ enum BwdBar {
   BB_SDP = 7,     // +buffer (2): S^T and dP^T in tensor memory
   BB_PDS = 9,     // +buffer (2): P^T, dS^T written (count 256)
   BB_DQ = 11,     // +buffer (2): dQ^T in tensor memory
-  BB_DQFREE = 13, // +buffer (2): dQ^T read out and the dS^T smem buffer's columns summed (count 128)
+  BB_DQFREE = 13, // +buffer (2): dQ^T read out of tensor memory (count 128)
   BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
   BB_BDONE = 16,  // every MMA of warp 13 retired
   BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
-  BB_DSFREE = 19, // +buffer (2): dQ staged over the dS^T smem buffer has been read out (count 4)
+  BB_DSFREE = 19, // +buffer (2): the dS^T smem buffer has been summed, and the dQ block staged
+                  // over it read out by the bulk engine (count 4)
 };
 
 // Barrier over `n` threads that also ORs a predicate across them: every thread gets the
@@ -506,6 +507,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars[BB_DSFREE + (x ^ 1)]);
       }
       staged = false;
+      // dQ^T first, so that dP^T of g + 2 can follow as early as possible; the row sums below
+      // read the dS^T buffer, which the elementwise warps overwrite only after DSFREE.
+      ok = ok && mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      uint32_t r0[32], r1[32], rv = 0;
+      if (ok) {  // a failed wait still reaches the readout barrier below, where all four warps stop
+        tmem_ld32(tX + 64, r0);
+        tmem_ld32(tX + 96, r1);
+        tmem_ld_wait();
+      }
+      if (kExactSums && wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
+        const float* rs = rpart + (g % 3) * 4 * kHalf + ln;
+        rv = __float_as_uint((rs[0] + rs[kHalf]) + (rs[2 * kHalf] + rs[3 * kHalf]));
+      }
+      tc_fence_before();
+      if (ok) mbar_arrive(&bars[BB_DQFREE + x]);  // dQ^T is in registers
       float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
       if (!kExactSums && ok) {
         const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
@@ -531,20 +549,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane, (a.x + bq.x) + (c.x + d2.x));
         atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane + 1, (a.y + bq.y) + (c.y + d2.y));
       }
-      ok = mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r0[32], r1[32], rv = 0;
-      tmem_ld32(tX + 64, r0);
-      tmem_ld32(tX + 96, r1);
-      tmem_ld_wait();
-      if (kExactSums && wq < 2) {  // R of the half-tile's 64 queries: the four lane quarters' partials (slot g % 3)
-        const float* rs = rpart + (g % 3) * 4 * kHalf + ln;
-        rv = __float_as_uint((rs[0] + rs[kHalf]) + (rs[2 * kHalf] + rs[3 * kHalf]));
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[BB_DQFREE + x]);  // dQ^T is in registers and the dS^T buffer has been summed
       if (kExactSums && wq < 2) atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + ln, __uint_as_float(rv));
       if (wq * 32 < D) {
         // dQ[q0 + i][32 wq + lane] += dQ^T[32 wq + lane][i], as two blocks of 32 queries x 32
@@ -597,8 +601,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* rh = dlt + kHalf;
       float* rsum = reinterpret_cast<float*>(sm + L::kRsum) + ((g % 3) * 4 + wq) * kHalf;
       const float baseI_hi = recs[(size_t)I * kColRec + kTile], baseI_lo = recs[(size_t)I * kColRec + kTile + 1];
-      // SDP_g also orders this half-tile after the readout of g-2 (warp 13 waited for it
-      // before dP^T_g), which freed the dS^T smem buffer x.
       ok = mbar_wait(&bars[BB_SDP + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA) &&
            mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05 loads / stores below are warp-collective

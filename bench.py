@@ -55,14 +55,38 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(src: str) -> str:
+    """C / CUDA source with comments removed and whitespace runs collapsed (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; an ncu traffic figure is only reported for the build it was taken on."""
+    """Hash of the CUDA sources' code (comments and layout ignored); an ncu traffic figure is
+    only reported for the code it was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "forget_gated_softmax_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -105,11 +105,13 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
 //                 buffer, dP^T_g = V dO_g^T once dQ^T_g-2 has been read out.
 //   warp 14       dV += P^T_g dO_g, dK += dS^T_g Q_g, then dQ^T_g = K^T dS^T_g (dS^T from
 //                 shared memory) once the elementwise warps are done with g.
-//                 (A single thread issues tcgen05.mma at a bounded rate, hence two.)
+//                 (Two issuers measured faster than one: each group of MMAs waits on a
+//                 different part of the pipeline.)
 //   8 elementwise P^T, dS^T of g (thread = key row x 32 queries); dS^T also goes to a
 //     warps        swizzled shared-memory buffer, the B operand of dQ^T.
-//   4 readout     the row sums R_g of dS (see below), then copy dQ^T_g out of tensor
-//     warps       memory and reduce it into the fp32 dQ accumulator.
+//   4 readout     copy dQ^T_g out of tensor memory (releasing its columns), the row sums
+//     warps       R_g of dS (see below), then add dQ into the fp32 accumulator: 4 KB
+//                 blocks staged in shared memory, added in L2 by the bulk-copy engine.
 //   1 producer    K_J, V_J once; Q, dO, Delta, rho half-tiles through 3 stages.
 // CTAs are scheduled in groups of kHeadGroup heads (see the kernel).
 // The gate gradient needs R_i = sum_j dS_ij and C_j = sum_i dS_ij from the same

@@ -399,6 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return true;
         };
+        if (has1 && s >= first0 && s + 1 < end0 && s + 1 < end1) {
+          // Both tiles take part in this step and the next: straight-line issue.
+          ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
+               mbar_wait(&bars[B_PFULL + 0], (s - first0) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, st, s > first0);
+          ok = mbar_wait(&bars[B_KFULL + nst], ((s + 1) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, nst);
+          umma_commit(&bars[B_SFULL + 0]);
+          ok = mbar_wait(&bars[B_PFULL + 1], s & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, st, s > 0);
+          issue_s(1, nst);
+          umma_commit(&bars[B_SFULL + 1]);
+          umma_commit(&bars[B_VEMPTY + st]);
+          umma_commit(&bars[B_KEMPTY + nst]);
+          continue;
+        }
         ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
         for (int k = 0; k < 2 && ok; ++k) {
           if (!active[k]) continue;

@@ -428,8 +428,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t tX = tbase + 128 * x;
           const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb;
           ok = mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-          // S^T_g overwrites P^T / dS^T of g-2, read by warp 14's dV / dK of g-2
-          if (ok && g >= 2) ok = mbar_wait(&bars[BB_KVD + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+          // S^T_g overwrites P^T / dS^T of g-2, read by warp 14's dV / dK of g-2. (For g < 2 the
+          // parity is 1: the phase before a fresh barrier's first counts as complete, so the
+          // wait returns at once and the issue path has no branch on g.)
+          if (ok) ok = mbar_wait(&bars[BB_KVD + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_ss(tX, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQs + qoff, 16, 1024), idSP, ks > 0);
           }
           // dP^T_g overwrites dQ^T of g-2, which the readout warps must have copied out
-          if (g >= 2) ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll

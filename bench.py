@@ -368,7 +368,8 @@ def run_fox(args, rank: int, world: int, local_rank: int):
         "gate_base_scan": ("hbm", w.B * w.H * ((w.N + 127) // 128) * (4 + 16)),
         "bwd_rows": ("hbm", w.tokens * (2 * w.d * 2 + 4 + 4 + 4 + 4 + 4 * w.d)),  # O, dO, lse, rowloc in; delta, rho, dQ-acc zero out
         "bwd_dq": ("hbm", w.tokens * w.d * (4 + 2)),
-        "bwd_gate": ("hbm", w.tokens * (4 + 4 + 4)),
+        "bwd_gate_blocks": ("hbm", w.tokens * (4 + 4)),  # R, C in
+        "bwd_gate": ("hbm", w.tokens * (4 + 4 + 4 + 4)),  # R, C, z in; dz out
     }
     kernels = {}
     for name, ms in per.items():
@@ -525,6 +526,40 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     }
     assert fox.fox_check_error(ws_f) == 0, "device-side error"
     del xg
+
+    # The gate steps alone on a large synthetic (B64 H32 N16384: 134 MB of z), where they are
+    # not launch-bound: the scan (log-sigmoid, 128-token tile scans, fp64 tile bases) into the
+    # workspace, and the gate gradient from the row and column sums of dS.
+    GB, GN, GH = 64, 16384, 32
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    zl = 2.0 + torch.randn((GB, GN, GH), generator=gen, device="cuda", dtype=torch.float32)
+    Rl = torch.randn((GB, GH, GN), generator=gen, device="cuda", dtype=torch.float32)
+    Cl = torch.randn((GB, GH, GN), generator=gen, device="cuda", dtype=torch.float32)
+    dzl = torch.empty_like(zl)
+    pg = fox.make_params(GB, GN, GH, 64)
+    ws_g = fox.workspace(fox.fox_gate_scan_workspace_bytes(pg), "cuda")
+    big = GB * GN * GH
+    peak_hbm = measured_peaks()[0]["hbm_gbs"]
+    scan_res = timed_variant(fox, torch, stream, lambda: fox.fox_gate_scan(zl, want_c=False, ws=ws_g, stream=stream),
+                             10, 0.0)
+    scan_ms = sum(scan_res["kernel_ms_per_step"].values())
+    scan_bytes = big * (4 + 4 + 4) + GB * GH * ((GN + 127) // 128) * 4 * 5  # z in; local and column terms out; tiles
+    ws_gb = fox.workspace(fox.fox_gate_bwd_workspace_bytes(pg), "cuda")
+    grad_res = timed_variant(fox, torch, stream, lambda: fox.fox_gate_bwd(zl, Rl, Cl, dz=dzl, ws=ws_gb, stream=stream),
+                             10, 0.0)
+    grad_ms = sum(grad_res["kernel_ms_per_step"].values())
+    grad_bytes = big * (4 + 4 + 4 + 4)  # R, C, z in; dz out (the block-sum pass re-reads R and C)
+    extra["gate_steps_large"] = {
+        "shape": f"B{GB} H{GH} N{GN} (z ~ N(2,1) fp32, R, C ~ N(0,1))",
+        "scan": {"ms": scan_ms, "kernel_ms": scan_res["kernel_ms_per_step"],
+                 "achieved": scan_bytes / (scan_ms * 1e-3) / 1e9, "unit": "GB/s", "bound": "hbm",
+                 "frac": scan_bytes / (scan_ms * 1e-3) / 1e9 / peak_hbm},
+        "gate_grad": {"ms": grad_ms, "kernel_ms": grad_res["kernel_ms_per_step"],
+                      "achieved": grad_bytes / (grad_ms * 1e-3) / 1e9, "unit": "GB/s", "bound": "hbm",
+                      "frac": grad_bytes / (grad_ms * 1e-3) / 1e9 / peak_hbm},
+    }
+    del zl, Rl, Cl, dzl, ws_g, ws_gb
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -49,6 +49,10 @@ EXPORTS = (
     "fox_tile_span",
     "fox_gate_proj",
     "fox_fwd_xgate",
+    "fox_gate_scan",
+    "fox_gate_scan_workspace_bytes",
+    "fox_gate_bwd",
+    "fox_gate_bwd_workspace_bytes",
 )
 
 
@@ -119,6 +123,14 @@ def lib() -> ctypes.CDLL:
         L.fox_fwd_noalloc.restype = i
         L.fox_noalloc_scratch_bytes.argtypes = []
         L.fox_noalloc_scratch_bytes.restype = sz
+        L.fox_gate_scan_workspace_bytes.argtypes = [pp]
+        L.fox_gate_scan_workspace_bytes.restype = sz
+        L.fox_gate_scan.argtypes = [pp, vp, vp, vp, sz, vp]
+        L.fox_gate_scan.restype = i
+        L.fox_gate_bwd_workspace_bytes.argtypes = [pp]
+        L.fox_gate_bwd_workspace_bytes.restype = sz
+        L.fox_gate_bwd.argtypes = [pp, vp, vp, vp, vp, vp, sz, vp]
+        L.fox_gate_bwd.restype = i
         L.fox_trace_begin.argtypes = []
         L.fox_trace_begin.restype = i
         L.fox_trace_end.argtypes = [ctypes.POINTER(fox_trace_record), i]
@@ -301,6 +313,56 @@ def fox_window(z, eps: float, *, window=None, ws=None, stream=None):
     if st != 0:
         raise FoxError(st, "fox_window")
     return window
+
+
+def fox_gate_scan_workspace_bytes(params: fox_params) -> int:
+    return int(lib().fox_gate_scan_workspace_bytes(ctypes.byref(params)))
+
+
+def fox_gate_scan(z, *, bias_from_j: bool = False, c=None, want_c: bool = True, ws=None, stream=None):
+    """The gate step alone: z [B, N, H] fp32 -> the cumulative log gate c [B, N, H] fp32
+    (c_t = sum_{l<=t} log sigmoid(z_l)); with want_c=False only the workspace's gate terms
+    are formed (what fox_fwd does first) and None is returned."""
+    torch = _torch()
+    B, N, H = z.shape
+    params = make_params(B, N, H, 64, FOX_DTYPE_BF16, 0.0, bias_from_j)
+    if want_c and c is None:
+        c = torch.empty((B, N, H), dtype=torch.float32, device=z.device)
+    if ws is None:
+        ws = workspace(fox_gate_scan_workspace_bytes(params), z.device)
+    if not z.is_contiguous() or (want_c and not c.is_contiguous()):
+        raise ValueError("fox_gate_scan needs contiguous tensors")
+    st = lib().fox_gate_scan(ctypes.byref(params), _ptr(z), _ptr(c) if want_c else None, _ptr(ws), ws.numel(),
+                             _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_gate_scan")
+    return c if want_c else None
+
+
+def fox_gate_bwd_workspace_bytes(params: fox_params) -> int:
+    return int(lib().fox_gate_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def fox_gate_bwd(z, R, C, *, bias_from_j: bool = False, dz=None, ws=None, stream=None):
+    """Gate gradient from the row / column sums of dS: z [B, N, H] fp32, R and C [B, H, N] fp32
+    -> dz [B, N, H] fp32 (suffix sums of R - C, plus C under bias_from_j, times sigmoid(-z))."""
+    torch = _torch()
+    B, N, H = z.shape
+    params = make_params(B, N, H, 64, FOX_DTYPE_BF16, 0.0, bias_from_j)
+    if tuple(R.shape) != (B, H, N) or tuple(C.shape) != (B, H, N):
+        raise ValueError("fox_gate_bwd: R and C must be [B, H, N]")
+    if dz is None:
+        dz = torch.empty((B, N, H), dtype=torch.float32, device=z.device)
+    if ws is None:
+        ws = workspace(fox_gate_bwd_workspace_bytes(params), z.device)
+    for t in (z, R, C, dz):
+        if not t.is_contiguous():
+            raise ValueError("fox_gate_bwd needs contiguous tensors")
+    st = lib().fox_gate_bwd(ctypes.byref(params), _ptr(z), _ptr(R), _ptr(C), _ptr(dz), _ptr(ws), ws.numel(),
+                            _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_gate_bwd")
+    return dz
 
 
 def fox_gate_proj(x, w_f, b_f, *, bias_from_j: bool = False, z=None, ws=None, stream=None):

@@ -389,6 +389,58 @@ fox_status fox_tile_span(const fox_params* p, const void* q, const void* k, cons
   return FOX_OK;
 }
 
+// Shape and flag checks of the gate-only calls (d, dtype, scale and the attention flags unused).
+static fox_status check_gate_params(const fox_params* p) {
+  if (!p || p->B < 0 || p->N < 0 || p->H < 0) return FOX_ERR_INVALID_ARG;
+  if (p->bias_from_j != 0 && p->bias_from_j != 1) return FOX_ERR_INVALID_ARG;
+  const long long BH = (long long)p->B * p->H;
+  if (BH > kMaxTokens || (long long)p->N > kMaxTokens - 2 * kTile || BH * (long long)p->N > kMaxTokens)
+    return FOX_ERR_INVALID_ARG;
+  return FOX_OK;
+}
+
+size_t fox_gate_scan_workspace_bytes(const fox_params* p) {
+  if (check_gate_params(p) != FOX_OK) return 0;
+  return gate_layout(p->B, p->N, p->H).end;
+}
+
+fox_status fox_gate_scan(const fox_params* p, const float* z, float* c, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  fox_status st = check_gate_params(p);
+  if (st != FOX_OK) return st;
+  if (p->B == 0 || p->H == 0 || p->N == 0) return FOX_OK;
+  if (!z || !aligned(z, 4) || (c && !aligned(c, 4))) return FOX_ERR_INVALID_ARG;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  st = check_workspace(workspace, workspace_bytes, g.end);
+  if (st != FOX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  if (c && launch_gate_cumulative(workspace, g, p->B, p->N, p->H, c, s) != cudaSuccess) return FOX_ERR_CUDA;
+  return FOX_OK;
+}
+
+size_t fox_gate_bwd_workspace_bytes(const fox_params* p) {
+  if (check_gate_params(p) != FOX_OK) return 0;
+  const size_t nT = ((size_t)p->N + kTile - 1) / kTile;
+  const size_t bytes = sizeof(float) * (size_t)p->B * p->H * nT;
+  return bytes < 256 ? 256 : align_up(bytes, 256);
+}
+
+fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, const float* C, float* dz,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  fox_status st = check_gate_params(p);
+  if (st != FOX_OK) return st;
+  if (p->B == 0 || p->H == 0 || p->N == 0) return FOX_OK;
+  if (!z || !R || !C || !dz || !aligned(z, 4) || !aligned(R, 4) || !aligned(C, 4) || !aligned(dz, 4))
+    return FOX_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, fox_gate_bwd_workspace_bytes(p));
+  if (st != FOX_OK) return st;
+  return launch_gate_bwd(p->B, p->N, p->H, p->N, p->bias_from_j, C, R, z, dz, static_cast<float*>(workspace),
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FOX_OK
+             : FOX_ERR_CUDA;
+}
+
 size_t fox_window_workspace_bytes(const fox_params* p) {
   if (!p || p->B < 0 || p->N < 0 || p->H < 0) return 0;
   if ((long long)p->B * p->H > kMaxTokens || (long long)p->B * p->H * (long long)p->N > kMaxTokens) return 0;

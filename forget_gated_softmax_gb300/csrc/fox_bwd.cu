@@ -719,51 +719,115 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Np
 }
 
 // ---------------------------------------------------------- gate backward
-// One CTA (1024 threads) per (b, h): reverse inclusive scan of the column
-// sums minus the column sums in chunks of 1024, from the end of the sequence.
-__global__ void __launch_bounds__(1024) bwd_gate_kernel(int N, int H, int Npad, int bias_from_j,
-                                                       const float* __restrict__ colsum,
-                                                       const float* __restrict__ rowsum, const float* __restrict__ z,
-                                                       float* __restrict__ dz) {
-  __shared__ float wsum[32];
-  const int bh = blockIdx.x;
-  const int b = bh / H, h = bh % H;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* C = colsum + (size_t)bh * Npad;
-  const float* R = rowsum + (size_t)bh * Npad;
-  float carry = 0.f;
-  const int nchunks = (N + 1023) / 1024;
-  for (int ck = nchunks - 1; ck >= 0; --ck) {
-    // element t = ck*1024 + 1023 - tid, so the scan in tid order is a suffix scan in t
-    const int t = ck * 1024 + 1023 - tid;
-    const float c = t < N ? C[t] : 0.f;
-    float x = t < N ? R[t] - c : 0.f;
+// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz_t = d a_t sigmoid(-z_t), in two
+// launches so that the loads of R, C, z and dz are coalesced and every SM takes part:
+//   1. gate_grad_block_kernel: warp per (b h, 128-token block): the block's sum of R - C;
+//   2. gate_grad_final_kernel: CTA per (128-token block, b, 32 heads): the carry from the
+//      later blocks (summed in fp64), the suffix scan inside the block, then dz over
+//      (token, head) so that the [B, N, H] accesses run along the heads.
+// R and C rows hold `stride` floats per (b, h); tokens past N count as 0.
+__global__ void __launch_bounds__(256) gate_grad_block_kernel(int BH, int N, int nT, int stride,
+                                                             const float* __restrict__ colsum,
+                                                             const float* __restrict__ rowsum,
+                                                             float* __restrict__ blocktot) {
+  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (long long)BH * nT) return;
+  const size_t bh = (size_t)(wid / nT);
+  const int k = (int)(wid % nT);
+  const float* R = rowsum + bh * stride;
+  const float* C = colsum + bh * stride;
+  float x = 0.f;
+#pragma unroll
+  for (int e = 0; e < kTile / 32; ++e) {
+    const int t = k * kTile + e * 32 + lane;
+    if (t < N) x += R[t] - C[t];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  if (lane == 0) blocktot[bh * nT + k] = x;
+}
+
+__global__ void __launch_bounds__(256) gate_grad_final_kernel(int N, int H, int nT, int stride, int bias_from_j,
+                                                             const float* __restrict__ colsum,
+                                                             const float* __restrict__ rowsum,
+                                                             const float* __restrict__ blocktot,
+                                                             const float* __restrict__ z, float* __restrict__ dz) {
+  constexpr int kPer = kTile * 32 / 256;  // elements per thread of the (token, head) tile
+  __shared__ float xs[32][kTile + 1];     // [head][token]: R - C, then d a
+  __shared__ float cs[32][kTile + 1];     // C (bias_from_j)
+  __shared__ float carry[32];
+  const int k = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * 32;
+  const int nh = min(32, H - h0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = k * kTile;
+  {
+    // carry of head hh: the later blocks' totals, summed in fp64 by 8 threads
+    const int hh = threadIdx.x >> 3, part = threadIdx.x & 7;
+    double c = 0.0;
+    if (hh < nh) {
+      const float* tot = blocktot + ((size_t)b * H + h0 + hh) * nT;
+      for (int kk = k + 1 + part; kk < nT; kk += 8) c += (double)tot[kk];
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (part == 0 && hh < nh) carry[hh] = (float)c;
+  }
+  {
+    // R, C: thread e covers token e % 128 of head e / 128 (rows contiguous per head); loads first
+    float rv[kPer], cv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * 256, hh = e / kTile, t = e % kTile;
+      const bool in = hh < nh && t0 + t < N;
+      const size_t off = ((size_t)b * H + h0 + hh) * stride + t0 + t;
+      rv[u] = in ? rowsum[off] : 0.f;
+      cv[u] = in ? colsum[off] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * 256, hh = e / kTile, t = e % kTile;
+      xs[hh][t] = rv[u] - cv[u];
+      cs[hh][t] = cv[u];
+    }
+  }
+  __syncthreads();
+  for (int hh = warp; hh < nh; hh += 8) {
+    // lane holds tokens 4 lane .. 4 lane + 3: suffix inside the lane, then over the later lanes
+    float v[4], run = 0.f;
+#pragma unroll
+    for (int e = 3; e >= 0; --e) {
+      run += xs[hh][4 * lane + e];
+      v[e] = run;
+    }
+    float later = run;  // inclusive suffix over lanes lane .. 31 of the lane totals
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const float y = __shfl_down_sync(0xffffffffu, later, o);
+      if (lane + o < 32) later += y;
     }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      float w = wsum[lane];
+    const float base = later - run + carry[hh];  // lanes after this one, then the later blocks
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      wsum[lane] = w;
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * lane + e;
+      xs[hh][t] = bias_from_j ? v[e] + base + cs[hh][t] : v[e] + base;
     }
-    __syncthreads();
-    const float incl = x + (warp > 0 ? wsum[warp - 1] : 0.f) + carry;  // sum_{s >= t} (R_s - C_s)
-    if (t < N) {
-      const float da = bias_from_j ? incl + c : incl;
-      const float zt = z[((size_t)b * N + t) * H + h];
-      const float sig_neg = 1.f / (1.f + expf(zt));  // sigmoid(-z); 0 at z = +inf
-      dz[((size_t)b * N + t) * H + h] = da * sig_neg;
+  }
+  __syncthreads();
+  {
+    // dz over (token, head), heads fastest: the [B, N, H] loads and stores run along the heads
+    float zv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * 256, t = e >> 5, hh = e & 31;
+      zv[u] = (hh < nh && t0 + t < N) ? z[((size_t)b * N + t0 + t) * H + h0 + hh] : 0.f;
     }
-    carry += wsum[31];
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * 256, t = e >> 5, hh = e & 31;
+      if (hh < nh && t0 + t < N)
+        dz[((size_t)b * N + t0 + t) * H + h0 + hh] = xs[hh][t] / (1.f + expf(zv[u]));  // d a sigmoid(-z)
+    }
   }
 }
 
@@ -827,14 +891,32 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  {
-    TraceScope trace("bwd_gate", s);
-    bwd_gate_kernel<<<g.BH, 1024, 0, s>>>(a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz);
-  }
-  return cudaGetLastError();
+  // the gate scan's tile totals are consumed by now: their buffer holds the block sums of R - C
+  return launch_gate_bwd(a.B, a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz,
+                         reinterpret_cast<float*>(a.ws + g.tiletot), s);
 }
 
 }  // namespace
+
+cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
+                            const float* rowsum, const float* z, float* dz, float* blocktot, cudaStream_t s) {
+  const long long BH = (long long)B * H;
+  if (BH == 0 || N == 0) return cudaSuccess;
+  const int nT = (N + kTile - 1) / kTile;
+  {
+    TraceScope trace("bwd_gate_blocks", s);
+    gate_grad_block_kernel<<<(unsigned)((BH * nT + 7) / 8), 256, 0, s>>>((int)BH, N, nT, stride, colsum, rowsum,
+                                                                          blocktot);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    TraceScope trace("bwd_gate", s);
+    gate_grad_final_kernel<<<dim3((unsigned)nT, (unsigned)B, (unsigned)((H + 31) / 32)), 256, 0, s>>>(
+        N, H, nT, stride, bias_from_j, colsum, rowsum, blocktot, z, dz);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w, const CUtensorMap* maps,
                             cudaStream_t s) {

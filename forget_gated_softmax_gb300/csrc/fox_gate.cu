@@ -314,6 +314,36 @@ cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const floa
   return cudaGetLastError();
 }
 
+namespace {
+// c[b,t,h] = (base_T + local_t) / log2 e, thread per (b, t, h): the output is coalesced over heads.
+__global__ void __launch_bounds__(256) gate_cumulative_kernel(int B, int N, int H, int nT, int Npad,
+                                                              const float* __restrict__ rowloc,
+                                                              const float* __restrict__ colrec, float* __restrict__ c) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)B * N * H) return;
+  const int h = (int)(idx % H);
+  const long long bt = idx / H;
+  const int t = (int)(bt % N), b = (int)(bt / N);
+  const size_t bh = (size_t)b * H + h;
+  const float* rec = colrec + (bh * nT + t / kTile) * kColRec;
+  const double v = (double)rec[kTile] + (double)rec[kTile + 1] + (double)rowloc[bh * Npad + t];
+  c[idx] = (float)(v / (double)kLog2e);
+}
+}  // namespace
+
+cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, int N, int H, float* c, cudaStream_t s) {
+  const char* base = static_cast<const char*>(ws);
+  const float* rowloc = reinterpret_cast<const float*>(base + g.rowloc);
+  const float* colrec = reinterpret_cast<const float*>(base + g.colrec);
+  const long long n = (long long)B * N * H;
+  if (n == 0) return cudaSuccess;
+  {
+    TraceScope trace("gate_cumulative", s);
+    gate_cumulative_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(B, N, H, g.nT, g.Npad, rowloc, colrec, c);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
                              cudaStream_t s) {
   char* base = static_cast<char*>(ws);

@@ -105,6 +105,12 @@ struct TraceScope {
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) ----
+// c[b,t,h] = (base_T + local_t) / log2 e from the gate terms in the workspace (fp64 sum, fp32 out).
+cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, int N, int H, float* c, cudaStream_t s);
+// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz = d a_t sigmoid(-z); R and C rows of
+// `stride` floats per (b, h); blocktot is scratch of B * H * ceil(N / 128) floats.
+cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
+                            const float* rowsum, const float* z, float* dz, float* blocktot, cudaStream_t s);
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
                              cudaStream_t s);
 

@@ -137,6 +137,39 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
                    size_t workspace_bytes, void* stream);
 
 /*
+ * The gate step alone: log f_t = log sigmoid(z_t) and its prefix sum along the
+ * sequence per (b, h) ("Forgetting Transformer (FoX) Attention" module source,
+ * ForgettingAttention.forward: sigmoid of the gate logits, log, cumsum), as the
+ * first launches of fox_fwd and fox_bwd compute them. The gate terms are left in
+ * the workspace; when c is not NULL the cumulative log gate
+ *   c[b,t,h] = sum_{l<=t} log sigmoid(z[b,l,h])   (natural log, fp32, [B,N,H])
+ * is written as well. No later call reads the workspace's gate terms (fox_fwd and
+ * fox_bwd always recompute them): the call exists to check and time this step on
+ * its own, at sizes where the attention itself would not fit. Only B, N, H and
+ * bias_from_j are read from p. z is [B,N,H] fp32. Workspace:
+ * fox_gate_scan_workspace_bytes(p) (the same as fox_fwd's for the same B, N, H).
+ */
+size_t fox_gate_scan_workspace_bytes(const fox_params* p);
+fox_status fox_gate_scan(const fox_params* p, const float* z, float* c, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * The gate gradient from the row and column sums of dS, the last step of
+ * fox_bwd: with R[b,h,t] = sum_j dS_tj and C[b,h,t] = sum_i dS_it,
+ *   d a_t = sum_{s>=t} (R_s - C_s)          (bias_from_j = 0)
+ *   d a_t = sum_{s>=t} (R_s - C_s) + C_t    (bias_from_j = 1)
+ *   dz[b,t,h] = d a_t * sigmoid(-z[b,t,h])  (d/dz log sigmoid(z) = sigmoid(-z))
+ * (chain rule through D_ij = c_i - c_j of the module's forward; the suffix form
+ * holds with or without the causal mask). R, C: [B,H,N] fp32, each (b, h) row
+ * contiguous; z, dz: [B,N,H] fp32. The sums are fp32 within 128-token blocks and
+ * fp64 across them. Only B, N, H and bias_from_j are read from p. Workspace (block
+ * sums): fox_gate_bwd_workspace_bytes(p).
+ */
+size_t fox_gate_bwd_workspace_bytes(const fox_params* p);
+fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, const float* C, float* dz,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Epsilon-effective window of every query row (foxwindow README, "The window is
  * a first-passage time"): with X_t = -log sigmoid(z_t) and L = ln(1/eps),
  *   window[b,i,h] = inf{ n >= 1 : X_i + X_{i-1} + ... + X_{i-n+1} > L },

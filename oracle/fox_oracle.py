@@ -55,6 +55,7 @@ __all__ = [
     "backward_head",
     "backward",
     "gate_grad_bruteforce",
+    "gate_grad_from_sums",
     "default_scale",
     "effective_window",
     "tile_pair_bound",
@@ -262,6 +263,27 @@ def gate_grad_bruteforce(dS: np.ndarray, bias_from_j: bool = False) -> np.ndarra
         split = t + 1 if bias_from_j else t  # keys j < split take +a_t (for rows i >= t)
         da[t] = dS[t:, :split].sum() - dS[:t, split:].sum()
     return da
+
+
+def gate_grad_from_sums(R, C, z, bias_from_j: bool = False) -> np.ndarray:
+    """dz of one (b, h) from the row sums R and column sums C of dS, z [N].
+
+    The gate part of backward_head on its own ([FoX-module] forward: D_ij = c_i - c_j
+    with c the cumsum of log sigmoid(z); chain rule):
+      j+1: d a_t = sum_{s>=t} (R_s - C_s);   j: d a_t = sum_{s>=t} (R_s - C_s) + C_t;
+      dz_t = d a_t * sigmoid(-z_t).
+    """
+    R = np.asarray(R, np.float64)
+    C = np.asarray(C, np.float64)
+    z = np.asarray(z, np.float64)
+    da = np.zeros(R.shape[0])
+    run = 0.0
+    for t in range(R.shape[0] - 1, -1, -1):  # the suffix sum, one term at a time
+        run += R[t] - C[t]
+        da[t] = run + C[t] if bias_from_j else run
+    with np.errstate(over="ignore"):
+        sig_neg = 1.0 / (1.0 + np.exp(z))  # sigmoid(-z); exactly 0 at z = +inf
+    return da * sig_neg
 
 
 def backward(q, k, v, z, dO, scale=None, bias_from_j=False, causal=True):

@@ -292,6 +292,25 @@ def test_gate_grad_suffix_scan_equals_double_sum(from_j):
     np.testing.assert_allclose(ex["da"], ora.gate_grad_bruteforce(ex["dS"], from_j), atol=1e-12)
 
 
+@pytest.mark.parametrize("from_j", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_gate_grad_from_sums_equals_double_sum(from_j, causal):
+    """The gate gradient from R and C alone (the standalone gate-backward step) equals the
+    brute-force double sum over the bias entries that hold a_t, for any dS (masked or not),
+    times sigmoid(-z) from scipy; z = +inf gives exactly 0."""
+    N = 37
+    r = np.random.default_rng(91 + 2 * from_j + causal)
+    dS = r.standard_normal((N, N))
+    if causal:
+        dS = np.tril(dS)
+    z = 1.0 + r.standard_normal(N)
+    z[5] = np.inf
+    dz = ora.gate_grad_from_sums(dS.sum(axis=1), dS.sum(axis=0), z, from_j)
+    want = ora.gate_grad_bruteforce(dS, from_j) * scipy.special.expit(-z)
+    np.testing.assert_allclose(dz, want, rtol=1e-12, atol=1e-12)
+    assert dz[5] == 0.0
+
+
 def test_row_shift_invariance_sums():
     """Adding a constant to a row of S leaves O unchanged, so every row sum of dS
     is 0 and the column sums add to 0; under j+1, a_0 enters no bias entry."""

@@ -175,9 +175,9 @@ enum BwdBar {
   BB_FULL = 1,    // +stage (3): Q, dO, Delta, rho of a half-tile landed
   BB_EMPTY = 4,   // +stage (3): the MMAs reading that stage retired
   BB_SDP = 7,     // +buffer (2): S^T and dP^T in tensor memory
-  BB_PDS = 9,     // +buffer (2): P^T, dS^T written (count 256)
+  BB_PDS = 9,     // +buffer (2): P^T, dS^T written (one arrival per elementwise warp)
   BB_DQ = 11,     // +buffer (2): dQ^T in tensor memory
-  BB_DQFREE = 13, // +buffer (2): dQ^T read out of tensor memory (count 128)
+  BB_DQFREE = 13, // +buffer (2): dQ^T read out of tensor memory (one arrival per readout warp)
   BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
   BB_BDONE = 16,  // every MMA of warp 13 retired
   BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
@@ -336,9 +336,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[BB_SDP + x], 1);
-      mbar_init(&bars[BB_PDS + x], 256);
+      mbar_init(&bars[BB_PDS + x], 8);
       mbar_init(&bars[BB_DQ + x], 1);
-      mbar_init(&bars[BB_DQFREE + x], 128);
+      mbar_init(&bars[BB_DQFREE + x], 4);
       mbar_init(&bars[BB_KVD + x], 1);
       mbar_init(&bars[BB_DSFREE + x], 4);
     }
@@ -527,7 +527,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         rv = __float_as_uint((rs[0] + rs[kHalf]) + (rs[2 * kHalf] + rs[3 * kHalf]));
       }
       tc_fence_before();
-      if (ok) mbar_arrive(&bars[BB_DQFREE + x]);  // dQ^T is in registers
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&bars[BB_DQFREE + x]);  // the warp's dQ^T is in registers
       float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
       if (!kExactSums && ok) {
         const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
@@ -639,7 +640,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[BB_PDS + x]);
+      __syncwarp();  // the warp's stores are ordered before the one arrival that speaks for it
+      if (lane == 0) mbar_arrive(&bars[BB_PDS + x]);
     }
     const int j = J * kTile + jr;
     {

@@ -87,7 +87,7 @@ enum Bar {
   B_VFULL = 5,    // +stage
   B_VEMPTY = 7,   // +stage
   B_SFULL = 9,    // +tile
-  B_PFULL = 11,   // +tile
+  B_PFULL = 11,   // +tile (one arrival per softmax warp)
   B_OFINAL = 13,  // +tile
   B_DONE = 15,
 };
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_VFULL + s], 1);
       mbar_init(&bars[B_VEMPTY + s], 1);
       mbar_init(&bars[B_SFULL + s], 1);
-      mbar_init(&bars[B_PFULL + s], 128);
+      mbar_init(&bars[B_PFULL + s], 4);
       mbar_init(&bars[B_OFINAL + s], 1);
     }
     mbar_init(&bars[B_DONE], 1);
@@ -488,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_PFULL + k]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_PFULL + k]);
       }
       for (int u = 1; u < nJk && ok; ++u) {
         const int s = first + u, st = s & 1;
@@ -548,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_PFULL + k]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_PFULL + k]);
       }
       if (ok) ok = mbar_wait(&bars[B_OFINAL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
       ok = __all_sync(0xffffffffu, ok);

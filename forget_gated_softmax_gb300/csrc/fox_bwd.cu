@@ -421,12 +421,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idQ = idesc_bf16(128, kHalf, true, true);     // dQ^T: A = K^T (MN-major), B = dS (MN-major)
       const uint32_t sK = smem_u32(sm + L::kK), sQ = smem_u32(sm + L::kQ), sdO = smem_u32(sm + L::kDO);
       bool ok = mbar_wait(&bars[BB_KV], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+      // Operand descriptors: the key-tile operands (K, V, K^T) are computed once; those of a
+      // half-tile stage or dS^T buffer are its base descriptor plus offset / 16, formed before
+      // each group so that the group's MMAs issue back to back. (Shared-memory addresses stay
+      // below 2^18, so the 14-bit start-address field of base + offset never carries.)
       if (warp == 13) {
         const uint32_t sV = smem_u32(sm + L::kV);
+        uint64_t aK[D / 16], aV[D / 16];
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;  // K / V tile: 128-row chunks
+          aK[ks] = sdesc_sw128(sK + koff, 16, 1024);
+          aV[ks] = sdesc_sw128(sV + koff, 16, 1024);
+        }
+        const uint64_t bQ0 = sdesc_sw128(sQ, 16, 1024), bdO0 = sdesc_sw128(sdO, 16, 1024);
         for (int g = 0; g < G && ok; ++g) {
           const int x = g & 1, st = g % kStages;
           const uint32_t tX = tbase + 128 * x;
-          const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb;
+          uint64_t bQ[D / 16], bdO[D / 16];
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t qoff = st * hb + (ks >> 2) * 8192 + (ks & 3) * 32;  // Q / dO half-tile: 64-row chunks
+            bQ[ks] = desc_plus(bQ0, qoff);
+            bdO[ks] = desc_plus(bdO0, qoff);
+          }
           ok = mbar_wait(&bars[BB_FULL + st], (g / kStages) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
           // S^T_g overwrites P^T / dS^T of g-2, read by warp 14's dV / dK of g-2. (For g < 2 the
           // parity is 1: the phase before a fresh barrier's first counts as complete, so the
@@ -435,21 +453,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;  // K / V tile: 128-row chunks
-            const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;   // Q / dO half-tile: 64-row chunks
-            umma_ss(tX, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQs + qoff, 16, 1024), idSP, ks > 0);
-          }
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tX, aK[ks], bQ[ks], idSP, ks > 0);
           // dP^T_g overwrites dQ^T of g-2, which the readout warps must have copied out
           ok = mbar_wait(&bars[BB_DQFREE + x], ((g - 2) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-            const uint32_t qoff = (ks >> 2) * 8192 + (ks & 3) * 32;
-            umma_ss(tX + 64, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(sdOs + qoff, 16, 1024), idSP, ks > 0);
-          }
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tX + 64, aV[ks], bdO[ks], idSP, ks > 0);
           umma_commit(&bars[BB_SDP + x]);
         }
       } else {
@@ -457,26 +467,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t sdS = smem_u32(sm + L::kDS), sZeros = smem_u32(sm + L::kZeros);
         // A = K^T: M = d channels (MN-major 64-wide chunks 16 KB apart; D = 64 pads the upper half with zeros)
         const uint32_t kt_lbo = D == 128 ? 16384u : sZeros - sK;
+        uint64_t aKt[kTile / 16];
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) aKt[ks] = sdesc_sw128(sK + ks * 2048, kt_lbo, 1024);
+        const uint64_t bdO0 = sdesc_sw128(sdO, 8192, 1024), bQ0 = sdesc_sw128(sQ, 8192, 1024);
+        const uint64_t bdS0 = sdesc_sw128(sdS, 16384, 1024);
         for (int g = 0; g < G && ok; ++g) {
           const int x = g & 1, st = g % kStages;
           const uint32_t tX = tbase + 128 * x;
-          const uint32_t sQs = sQ + st * hb, sdOs = sdO + st * hb, sdSx = sdS + x * 16384;
+          uint64_t bdO[kHalf / 16], bQ[kHalf / 16], bdS[kTile / 16];
+#pragma unroll
+          for (int ks = 0; ks < kHalf / 16; ++ks) {
+            bdO[ks] = desc_plus(bdO0, st * hb + ks * 2048);
+            bQ[ks] = desc_plus(bQ0, st * hb + ks * 2048);
+          }
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) bdS[ks] = desc_plus(bdS0, x * 16384 + ks * 2048);
           ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kHalf / 16; ++ks)  // dV += P^T dO (K = 64 queries)
-            umma_ts(tdV, tX + pds_col(ks), sdesc_sw128(sdOs + ks * 2048, 8192, 1024), idKV, (g > 0 || ks > 0) ? 1u : 0u);
+            umma_ts(tdV, tX + pds_col(ks), bdO[ks], idKV, (g > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < kHalf / 16; ++ks)  // dK += dS^T Q
-            umma_ts(tdK, tX + pds_col(ks) + 16, sdesc_sw128(sQs + ks * 2048, 8192, 1024), idKV,
-                    (g > 0 || ks > 0) ? 1u : 0u);
+            umma_ts(tdK, tX + pds_col(ks) + 16, bQ[ks], idKV, (g > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bars[BB_KVD + x]);
           umma_commit(&bars[BB_EMPTY + st]);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)  // dQ^T = K^T dS^T (K = 128 keys) over [64,128)
-            umma_ss(tX + 64, sdesc_sw128(sK + ks * 2048, kt_lbo, 1024), sdesc_sw128(sdSx + ks * 2048, 16384, 1024),
-                    idQ, ks > 0);
+            umma_ss(tX + 64, aKt[ks], bdS[ks], idQ, ks > 0);
           umma_commit(&bars[BB_DQ + x]);
         }
       }

@@ -350,23 +350,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       const uint32_t tS[2] = {tbase, tbase + 128};
       const uint32_t tO[2] = {tbase + 256, tbase + 256 + D};
-      const uint32_t sQ[2] = {smem_u32(sm + L::kQ0), smem_u32(sm + L::kQ1)};
-      const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+      // Descriptors of each operand tile's base. Shared-memory addresses stay below 2^18, so
+      // the 14-bit start-address field of base + offset never carries: an operand at a byte
+      // offset is the base descriptor plus offset / 16.
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + L::kQ0), 16, 1024);
+      const uint64_t dQ1 = sdesc_sw128(smem_u32(sm + L::kQ1), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sm + L::kK), 16, 1024);
+      const uint64_t dK1 = sdesc_sw128(smem_u32(sm + L::kK + tb), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sm + L::kV), 16384, 1024);
+      const uint64_t dV1 = sdesc_sw128(smem_u32(sm + L::kV + tb), 16384, 1024);
       const int first[2] = {first0, 0};
       const int end[2] = {end0, end1};
       const bool active[2] = {true, has1};
+      // Every operand descriptor of the S and P V groups, computed once.
+      uint64_t dA[2][D / 16], dB[2][D / 16], dVs[2][kTile / 16];
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+        dA[0][ks] = dQ0 + off;
+        dA[1][ks] = dQ1 + off;
+        dB[0][ks] = dK0 + off;
+        dB[1][ks] = dK1 + off;
+      }
+#pragma unroll
+      for (int ks = 0; ks < kTile / 16; ++ks) {
+        dVs[0][ks] = dV0 + static_cast<uint64_t>((ks * 2048) >> 4);
+        dVs[1][ks] = dV1 + static_cast<uint64_t>((ks * 2048) >> 4);
+      }
       auto issue_s = [&](int k, int st) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          umma_ss(tS[k], sdesc_sw128(sQ[k] + off, 16, 1024), sdesc_sw128(sK + st * tb + off, 16, 1024), idS,
-                  ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[k], dA[k][ks], st ? dB[1][ks] : dB[0][ks], idS, ks > 0);
       };
       auto issue_pv = [&](int k, int st, bool acc) {
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
-          const uint64_t dv = sdesc_sw128(sV + st * tb + ks * 2048, 16384, 1024);
+          const uint64_t dv = st ? dVs[1][ks] : dVs[0][ks];
           if (kDelta) {  // P = hi + lo: chunk ks/2 holds hi at +0 and lo at +16 columns
             const uint32_t a = tS[k] + 32 * (ks >> 1) + 8 * (ks & 1);
             umma_ts(tO[k], a, dv, idO, (acc || ks > 0) ? 1u : 0u);

@@ -225,6 +225,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Descriptor of an operand `off_bytes` past the one `d` describes, for addresses that stay
+// inside shared memory (below 2^18): the start-address field (bits 0-13, in 16-byte units)
+// then never carries, so only the low word changes.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t d, uint32_t off_bytes) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (off_bytes >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)     // D format: f32

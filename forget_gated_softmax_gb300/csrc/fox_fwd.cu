@@ -244,6 +244,12 @@ __device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap
   return s.x + s.y;
 }
 
+// A stage index as a type, for code specialised on it.
+template <int V>
+struct StageC {
+  static constexpr int value = V;
+};
+
 template <int D, bool kDelta>
 __global__ void __launch_bounds__(kThreads, 1)
     fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -394,6 +400,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // One K-step of P V for Q tile k with the V descriptor dv.
+      auto pv_ks = [&](int k, int ks, bool acc, uint64_t dv) {
+        if (kDelta) {  // P = hi + lo: chunk ks/2 holds hi at +0 and lo at +16 columns
+          const uint32_t a = tS[k] + 32 * (ks >> 1) + 8 * (ks & 1);
+          umma_ts(tO[k], a, dv, idO, (acc || ks > 0) ? 1u : 0u);
+          umma_ts(tO[k], a + 16, dv, idO, 1u);
+        } else {
+          umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
       bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
                 mbar_wait(&bars[B_KFULL + 0], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
       if (ok) {
@@ -417,26 +433,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return true;
         };
-        if (has1 && s >= first0 && s + 1 < end0 && s + 1 < end1) {
-          // Both tiles take part in this step and the next: straight-line issue.
-          ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
-               mbar_wait(&bars[B_PFULL + 0], (s - first0) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
-          if (!ok) break;
+        // Both tiles take part in this step and the next: straight-line issue, specialised
+        // on the stage parity so that every descriptor and barrier address is fixed.
+        auto straight = [&](auto stage) -> bool {
+          constexpr int ST = decltype(stage)::value, NST = ST ^ 1;
+          bool ok = mbar_wait(&bars[B_VFULL + ST], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
+                    mbar_wait(&bars[B_PFULL + 0], (s - first0) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+          if (!ok) return false;
           tc_fence_after();
-          issue_pv(0, st, s > first0);
-          ok = mbar_wait(&bars[B_KFULL + nst], ((s + 1) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
-          if (!ok) break;
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) pv_ks(0, ks, s > first0, dVs[ST][ks]);
+          ok = mbar_wait(&bars[B_KFULL + NST], ((s + 1) >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+          if (!ok) return false;
           tc_fence_after();
-          issue_s(0, nst);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[0], dA[0][ks], dB[NST][ks], idS, ks > 0);
           umma_commit(&bars[B_SFULL + 0]);
           ok = mbar_wait(&bars[B_PFULL + 1], s & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
-          if (!ok) break;
+          if (!ok) return false;
           tc_fence_after();
-          issue_pv(1, st, s > 0);
-          issue_s(1, nst);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) pv_ks(1, ks, s > 0, dVs[ST][ks]);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[1], dA[1][ks], dB[NST][ks], idS, ks > 0);
           umma_commit(&bars[B_SFULL + 1]);
-          umma_commit(&bars[B_VEMPTY + st]);
-          umma_commit(&bars[B_KEMPTY + nst]);
+          umma_commit(&bars[B_VEMPTY + ST]);
+          umma_commit(&bars[B_KEMPTY + NST]);
+          return true;
+        };
+        if (has1 && s >= first0 && s + 1 < end0 && s + 1 < end1) {
+          ok = (s & 1) ? straight(StageC<1>{}) : straight(StageC<0>{});
+          if (!ok) break;
           continue;
         }
         ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);

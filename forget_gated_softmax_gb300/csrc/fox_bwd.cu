@@ -23,6 +23,8 @@
 //                 C_j of dS (added into global accumulators)
 //   bwd_dq        dQ = scale * accumulator -> bf16
 //   bwd_gate      reverse prefix scan of (R - C) and the sigmoid chain rule -> dz
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,55 +44,86 @@ __device__ __forceinline__ size_t dq_offset(size_t bh, int Npad, int i, int e) {
 }
 
 // ------------------------------------------------------------------ rows
-// One warp per (b, i, h) with i in [0, Npad).
+// Delta_i = dO_i . O_i, the row offset rho_i and a cleared row sum for every row (b, i, h)
+// with i < N, taken in the [B, N, H] order of O, dO and LSE so that their loads are contiguous:
+// a warp takes 8 consecutive rows, D / 8 lanes per row, each lane one 16-byte piece of O and
+// of dO per row, all issued before the arithmetic. The padding rows N <= i < Npad of every
+// (b, h) get Delta = 0, rho = +inf and R = 0 from a grid-stride loop over the same threads.
+// (The dQ accumulator is zeroed by a memset before this kernel.)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int Npad, const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                                                       const float* __restrict__ rowloc, float* __restrict__ delta,
                                                       float* __restrict__ rho, float* __restrict__ rowsum,
-                                                      float* __restrict__ dqacc, int delta_ready) {
-  constexpr int E = D / 32;  // elements per lane
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const long long rows = (long long)B * Npad * H;
-  if (row >= rows) return;
-  const int h = (int)(row % H);
-  const long long bi = row / H;
-  const int i = (int)(bi % Npad);
-  const int b = (int)(bi / Npad);
-  const size_t bh = (size_t)b * H + h;
-  float acc = 0.f;
-  if (i < N) {
-    const size_t base = (((size_t)b * N + i) * H + h) * D + lane * E;
-    if (E == 4) {
-      const uint2 ov = *reinterpret_cast<const uint2*>(o + base);
-      const uint2 gv = *reinterpret_cast<const uint2*>(dO + base);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+                                                      int delta_ready) {
+  constexpr int LPR = D / 8;          // lanes per row
+  constexpr int RPI = 32 / LPR;       // rows per load instruction
+  constexpr int LOADS = 8 / RPI;      // loads per lane per tensor
+  const int lane = threadIdx.x & 31, sub = lane % LPR, grp = lane / LPR;
+  const long long rows = (long long)B * N * H;
+  const long long octet = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long row0 = octet * 8;
+  if (row0 < rows) {
+    uint4 ov[LOADS], gv[LOADS];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 a = __bfloat1622float2(o2[e]), c = __bfloat1622float2(g2[e]);
-        acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+    for (int k = 0; k < LOADS; ++k) {
+      const long long row = row0 + k * RPI + grp;
+      ov[k] = make_uint4(0u, 0u, 0u, 0u);
+      gv[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < rows) {
+        ov[k] = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
+        gv[k] = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
       }
-    } else {
-      const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-      const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
-      const float2 a = __bfloat1622float2(ov), c = __bfloat1622float2(gv);
-      acc = fmaf(a.x, c.x, a.y * c.y);
+    }
+    float acc[LOADS];
+#pragma unroll
+    for (int k = 0; k < LOADS; ++k) {
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[k]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[k]);
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(o2[e]), y = __bfloat1622float2(g2[e]);
+        sum = fmaf(x.x, y.x, fmaf(x.y, y.y, sum));
+      }
+      acc[k] = sum;
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int k = 0; k < LOADS; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+    // Lane m < 8 finishes row row0 + m: its sum sits in lane (m % RPI) * LPR, slot m / RPI.
+    // (B * N * H < 2^31, so the row index and its decode fit 32-bit arithmetic.)
+    const int m = lane & 7;
+    float dsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < LOADS; ++k) {
+      const float v = __shfl_sync(0xffffffffu, acc[k], (m % RPI) * LPR);
+      if (k == m / RPI) dsum = v;
+    }
+    const long long rowm = row0 + m;
+    if (lane < 8 && rowm < rows) {
+      const uint32_t row = static_cast<uint32_t>(rowm);
+      const uint32_t h = row % (uint32_t)H, t = row / (uint32_t)H;
+      const uint32_t i = t % (uint32_t)N, b = t / (uint32_t)N;
+      const size_t r = ((size_t)b * H + h) * Npad + i;
+      rowsum[r] = 0.f;
+      if (!delta_ready) delta[r] = dsum;
+      rho[r] = lse[row] * kLog2e - rowloc[r];
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  float* dq = dqacc + dq_offset<D>(bh, Npad, i, lane * E);
-#pragma unroll
-  for (int e = 0; e < E; ++e) dq[e] = 0.f;
-  if (lane == 0) {
-    rowsum[bh * Npad + i] = 0.f;
-    if (!delta_ready || i >= N) delta[bh * Npad + i] = i < N ? acc : 0.f;
-    rho[bh * Npad + i] =
-        i < N ? lse[((size_t)b * N + i) * H + h] * kLog2e - rowloc[bh * Npad + i] : __int_as_float(0x7f800000);
+  const long long pads = (long long)B * H * (Npad - N);
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < pads; q += (long long)gridDim.x * blockDim.x) {
+    const long long bh = q / (Npad - N);
+    const size_t r = (size_t)bh * Npad + N + (size_t)(q % (Npad - N));
+    rowsum[r] = 0.f;
+    delta[r] = 0.f;
+    rho[r] = __int_as_float(0x7f800000);
   }
 }
+
+// Rows per warp of the dQ conversion.
+constexpr int kRowWarp = 4;
 
 // ------------------------------------------------------------------ main
 // One CTA per (b, h, 128-key tile J). The query tiles I >= J (every I when not
@@ -715,28 +748,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ out
+// One warp per kRowWarp consecutive rows (b, i, h), i < N; loads first, then the stores.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Npad, float scale,
                                                     const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq) {
   constexpr int E = D / 32;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  using In = typename std::conditional<E == 4, float4, float2>::type;
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowWarp;
   const int lane = threadIdx.x & 31;
-  if (row >= (long long)B * N * H) return;
-  const int h = (int)(row % H);
-  const long long bi = row / H;
-  const int i = (int)(bi % N);
-  const int b = (int)(bi / N);
-  const float* src = dqacc + dq_offset<D>((size_t)b * H + h, Npad, i, lane * E);
-  __nv_bfloat16* dst = dq + (size_t)row * D + lane * E;
-  if (E == 4) {
-    const float4 v = *reinterpret_cast<const float4*>(src);
-    uint2 w;
-    w.x = pack_bf16x2(v.x * scale, v.y * scale);
-    w.y = pack_bf16x2(v.z * scale, v.w * scale);
-    *reinterpret_cast<uint2*>(dst) = w;
-  } else {
-    const float2 v = *reinterpret_cast<const float2*>(src);
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(v.x * scale, v.y * scale);
+  const long long rows = (long long)B * N * H;
+  In v[kRowWarp];
+#pragma unroll
+  for (int r = 0; r < kRowWarp; ++r) {
+    const uint32_t row = static_cast<uint32_t>(row0 + r < rows ? row0 + r : rows - 1);  // B * N * H < 2^31
+    const uint32_t h = row % (uint32_t)H, bi = row / (uint32_t)H;
+    const uint32_t i = bi % (uint32_t)N, b = bi / (uint32_t)N;
+    v[r] = *reinterpret_cast<const In*>(dqacc + dq_offset<D>((size_t)b * H + h, Npad, i, lane * E));
+  }
+#pragma unroll
+  for (int r = 0; r < kRowWarp; ++r) {
+    if (row0 + r >= rows) break;
+    __nv_bfloat16* dst = dq + (size_t)(row0 + r) * D + lane * E;
+    if constexpr (E == 4) {
+      uint2 w;
+      w.x = pack_bf16x2(v[r].x * scale, v[r].y * scale);
+      w.y = pack_bf16x2(v[r].z * scale, v[r].w * scale);
+      *reinterpret_cast<uint2*>(dst) = w;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(v[r].x * scale, v[r].y * scale);
+    }
   }
 }
 
@@ -868,10 +908,15 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   uint32_t* err = reinterpret_cast<uint32_t*>(a.ws);
   const long long rows = (long long)a.B * g.Npad * a.H;
   {
+    TraceScope trace("dq_zero", s);
+    if (cudaMemsetAsync(dqacc, 0, (size_t)rows * D * sizeof(float), s) != cudaSuccess) return cudaGetLastError();
+  }
+  {
     TraceScope trace("bwd_rows", s);
-    bwd_rows_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    const long long octets = ((long long)a.B * a.N * a.H + 7) / 8;  // 8 rows per warp, 8 warps per block
+    bwd_rows_kernel<D><<<(unsigned)((octets + 7) / 8), 256, 0, s>>>(
         a.B, a.N, a.H, g.Npad, static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        rowloc, delta, rho, rowsum, dqacc, a.delta_ready);
+        rowloc, delta, rho, rowsum, a.delta_ready);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -908,7 +953,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   const long long drows = (long long)a.B * a.N * a.H;
   {
     TraceScope trace("bwd_dq", s);
-    bwd_dq_kernel<D><<<(unsigned)((drows + 7) / 8), 256, 0, s>>>(a.B, a.N, a.H, g.Npad, a.scale, dqacc,
+    bwd_dq_kernel<D><<<(unsigned)((drows + 8 * kRowWarp - 1) / (8 * kRowWarp)), 256, 0, s>>>(a.B, a.N, a.H, g.Npad, a.scale, dqacc,
                                                                    static_cast<__nv_bfloat16*>(a.dq));
   }
   e = cudaGetLastError();

@@ -13,8 +13,8 @@
 //   contain a_t, instead of accumulating those row errors along the sequence.
 //
 // Kernels, in launch order (the gate scan of the forward runs first):
-//   bwd_rows      Delta_i, the row offset rho_i = LSE_i log2 e - l_i; zeroes the dQ
-//                 accumulator and the row sums
+//   (memset)      the dQ accumulator cleared
+//   bwd_rows      Delta_i, the row offset rho_i = LSE_i log2 e - l_i; clears the row sums
 //   bwd_main      one CTA per (b, h, 128-key tile J) over the query tiles I >= J
 //                 (all I when not causal), pipelined over 64-query half-tiles:
 //                 S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q and

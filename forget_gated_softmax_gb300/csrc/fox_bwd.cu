@@ -637,7 +637,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       staged = true;
     }
-    if (lane == 0) bulk_wait_all();  // every reduction has landed in the accumulator
+    // The bulk engine must have read every staged block before shared memory is released;
+    // the additions themselves complete before the kernel does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   } else {
     // ------------------------------------------------------ P^T, dS^T, epilogue
@@ -712,25 +714,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr int kCols = D / 2;
       const int e0 = ch * kCols;
       const uint32_t tdK = tbase + 256 + lane_off, tdV = tbase + 256 + D + lane_off;
+      // Two 32-column loads in flight per wait.
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t src = (which == 0 ? tdK : tdV) + e0;
         const float mul = which == 0 ? p.scale : 1.f;
         __nv_bfloat16* outp = which == 0 ? p.dk : p.dv;
 #pragma unroll
-        for (int c = 0; c < kCols; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(src + c, r);
+        for (int c = 0; c < kCols; c += 64) {
+          uint32_t r[2][32];
+          tmem_ld32(src + c, r[0]);
+          if (c + 32 < kCols) tmem_ld32(src + c + 32, r[1]);
           tmem_ld_wait();
-          if (j < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(outp + (((size_t)b * p.N + j) * p.H + h) * D + e0 + c);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (c + 32 * hh >= kCols || j >= p.N) continue;
+            uint4* dst = reinterpret_cast<uint4*>(outp + (((size_t)b * p.N + j) * p.H + h) * D + e0 + c + 32 * hh);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * mul, __uint_as_float(r[8 * q4 + 1]) * mul);
-              w.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * mul, __uint_as_float(r[8 * q4 + 3]) * mul);
-              w.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * mul, __uint_as_float(r[8 * q4 + 5]) * mul);
-              w.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * mul, __uint_as_float(r[8 * q4 + 7]) * mul);
+              w.x = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 0]) * mul, __uint_as_float(r[hh][8 * q4 + 1]) * mul);
+              w.y = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 2]) * mul, __uint_as_float(r[hh][8 * q4 + 3]) * mul);
+              w.z = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 4]) * mul, __uint_as_float(r[hh][8 * q4 + 5]) * mul);
+              w.w = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 6]) * mul, __uint_as_float(r[hh][8 * q4 + 7]) * mul);
               dst[q4] = w;
             }
           }

@@ -4,7 +4,7 @@
 // along the sequence), stored two-level so that the attention kernels can
 // form D_ij = c_i - c_j to fp32 accuracy at any sequence length:
 // tile-local fp32 sums (warp-shuffle scan over 128 tokens) plus per-tile
-// bases from an fp64 scan over tile totals.
+// bases from a double-float (about 48-bit) scan over tile totals.
 #include <cuda_runtime.h>
 
 #include "fox_internal.h"
@@ -61,32 +61,37 @@ __device__ __forceinline__ void scan_head_column(const float (*zs)[kHeadsPerPass
   if (lane == 31) tiletot[bh * nT + T] = incl[3];
 }
 
-// One CTA per (tile T, batch b); all heads of that tile. z rows of one token
-// are contiguous over heads, so the load is coalesced; each warp then scans
-// one head's 128 tokens.
+// One CTA per (tile T, batch b, group of kTileScanHeads heads). Each thread loads its
+// z values first (a warp reads 2 tokens x 16 heads, whole 32-byte sectors), then takes
+// the log-sigmoids; each warp then scans one or two heads' 128 tokens.
+constexpr int kTileScanHeads = 16;
+
 __global__ void __launch_bounds__(256) gate_tile_scan_kernel(const float* __restrict__ z, int B, int N, int H,
                                                              int nT, int Npad, int bias_from_j,
                                                              float* __restrict__ rowloc, float* __restrict__ colrec,
                                                              float* __restrict__ tiletot, uint32_t* err) {
   __shared__ float zs[kTile][kHeadsPerPass + 1];
-  const int T = blockIdx.x, b = blockIdx.y;
+  const int T = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * kTileScanHeads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (T == 0 && b == 0 && threadIdx.x == 0 && err) *err = 0u;  // each call starts with a clean error word
+  if (T == 0 && b == 0 && h0 == 0 && threadIdx.x == 0 && err) *err = 0u;  // each call starts with a clean error word
   const int t0 = T * kTile;
-  for (int h0 = 0; h0 < H; h0 += kHeadsPerPass) {
-    const int nh = min(kHeadsPerPass, H - h0);
-    __syncthreads();
-    for (int e = threadIdx.x; e < kTile * kHeadsPerPass; e += blockDim.x) {
-      const int r = e / kHeadsPerPass, c = e % kHeadsPerPass;
-      const int t = t0 + r;
-      float a = 0.f;  // tokens past the end contribute log f = 0
-      if (t < N && c < nh) a = log_sigmoid(z[((size_t)b * N + t) * H + h0 + c]) * kLog2e;
-      zs[r][c] = a;
-    }
-    __syncthreads();
-    for (int c = warp; c < nh; c += blockDim.x / 32)
-      scan_head_column(zs, c, lane, (size_t)b * H + h0 + c, T, N, nT, Npad, bias_from_j, rowloc, colrec, tiletot);
+  const int nh = min(kTileScanHeads, H - h0);
+  constexpr int kPer = kTile * kTileScanHeads / 256;  // values per thread
+  float v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = threadIdx.x + u * 256, r = e / kTileScanHeads, c = e % kTileScanHeads;
+    const int t = t0 + r;
+    v[u] = (t < N && c < nh) ? z[((size_t)b * N + t) * H + h0 + c] : INFINITY;  // log f = 0 past the end
   }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = threadIdx.x + u * 256;
+    zs[e / kTileScanHeads][e % kTileScanHeads] = log_sigmoid(v[u]) * kLog2e;
+  }
+  __syncthreads();
+  for (int c = warp; c < nh; c += 8)
+    scan_head_column(zs, c, lane, (size_t)b * H + h0 + c, T, N, nT, Npad, bias_from_j, rowloc, colrec, tiletot);
 }
 
 // ---------------------------------------------------------------- fused gate projection
@@ -241,30 +246,53 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   }
 }
 
-// One warp per (b, h): exclusive fp64 scan of the tile totals -> base_T,
-// stored as an fp32 hi/lo pair in each column record.
+// Double-float arithmetic (a value is hi + lo, two fp32 numbers; Knuth's TwoSum and
+// Dekker's FastTwoSum): about 48 significant bits from fp32 additions only.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb) + (a.lo + b.lo);
+  const float hi = s + e;
+  return DF{hi, e - (hi - s)};
+}
+
+// One warp per (b, h): exclusive scan of the tile totals -> base_T, in double-float,
+// stored as the hi/lo pair in each column record. The totals of up to 128 tiles are
+// loaded before the scan (4 per lane), so the loads overlap.
 __global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, const float* __restrict__ tiletot,
                                                              float* __restrict__ colrec) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= BH) return;
-  double carry = 0.0;
-  for (int T0 = 0; T0 < nT; T0 += 32) {
-    const int T = T0 + lane;
-    const double v = T < nT ? (double)tiletot[(size_t)warp * nT + T] : 0.0;
-    double incl = v;
+  DF carry{0.f, 0.f};
+  for (int T0 = 0; T0 < nT; T0 += 128) {
+    float v[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    for (int q = 0; q < 4; ++q) {
+      const int T = T0 + 32 * q + lane;
+      v[q] = T < nT ? tiletot[(size_t)warp * nT + T] : 0.f;
     }
-    const double base = carry + incl - v;
-    if (T < nT) {
-      float* rec = colrec + ((size_t)warp * nT + T) * kColRec;
-      const float hi = (float)base;
-      const float lo = (float)(base - (double)hi);
-      *reinterpret_cast<float4*>(rec + kTile) = make_float4(hi, lo, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int T = T0 + 32 * q + lane;
+      DF incl{v[q], 0.f};
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const DF y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+        if (lane >= o) incl = df_add(incl, y);
+      }
+      // exclusive prefix = carry + (inclusive - own value): the lane below's inclusive sum
+      DF below{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+      if (lane == 0) below = DF{0.f, 0.f};
+      const DF base = df_add(carry, below);
+      if (T < nT) {
+        float* rec = colrec + ((size_t)warp * nT + T) * kColRec;
+        *reinterpret_cast<float4*>(rec + kTile) = make_float4(base.hi, base.lo, 0.f, 0.f);
+      }
+      carry = df_add(carry, DF{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)});
     }
-    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 
@@ -351,7 +379,7 @@ cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_
   float* colrec = reinterpret_cast<float*>(base + g.colrec);
   float* tiletot = reinterpret_cast<float*>(base + g.tiletot);
   uint32_t* err = reinterpret_cast<uint32_t*>(base);
-  dim3 grid(g.nT, B);
+  dim3 grid(g.nT, B, (H + kTileScanHeads - 1) / kTileScanHeads);
   {
     TraceScope trace("gate_tile_scan", s);
     gate_tile_scan_kernel<<<grid, 256, 0, s>>>(z, B, N, H, g.nT, g.Npad, bias_from_j, rowloc, colrec, tiletot, err);

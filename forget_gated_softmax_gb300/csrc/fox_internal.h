@@ -18,7 +18,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   colrec[bh][T]   { kappa_j for j in tile T (tile-local column term:
 //                     inclusive for the j+1 convention, exclusive for the j convention;
 //                     +inf past the sequence end, which removes those keys from every row),
-//                     base_T hi, base_T lo, 0, 0 },  base_T = sum_{l < 128*T} a_l (fp64 scan, split hi+lo)
+//                     base_T hi, base_T lo, 0, 0 },  base_T = sum_{l < 128*T} a_l (double-float scan, hi+lo)
 //   tiletot[bh][T]  sum of a over tile T (fp32, scratch between the two gate kernels)
 // so that, for i in tile I and j in tile J, D_ij * log2 e = l_i - kappa_j + (base_I - base_J).
 // Tile-skip arrays (written only when skipping is requested):

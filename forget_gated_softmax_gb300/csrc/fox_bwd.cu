@@ -794,6 +794,16 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Np
 //      later blocks (summed in fp64), the suffix scan inside the block, then dz over
 //      (token, head) so that the [B, N, H] accesses run along the heads.
 // R and C rows hold `stride` floats per (b, h); tokens past N count as 0.
+// (hi, lo) += (bhi, blo) in double-float: Knuth's TwoSum on the high parts, the low parts
+// added in fp32, renormalised with Dekker's FastTwoSum (about 48 significant bits).
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float bhi, float blo) {
+  const float s = hi + bhi;
+  const float bb = s - hi;
+  const float e = (hi - (s - bb)) + (bhi - bb) + (lo + blo);
+  hi = s + e;
+  lo = e - (hi - s);
+}
+
 __global__ void __launch_bounds__(256) gate_grad_block_kernel(int BH, int N, int nT, int stride,
                                                              const float* __restrict__ colsum,
                                                              const float* __restrict__ rowsum,
@@ -830,16 +840,24 @@ __global__ void __launch_bounds__(256) gate_grad_final_kernel(int N, int H, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = k * kTile;
   {
-    // carry of head hh: the later blocks' totals, summed in fp64 by 8 threads
+    // carry of head hh: the later blocks' totals, summed by 8 threads in double-float (hi + lo
+    // fp32 pairs added with TwoSum), four loads issued before their additions
     const int hh = threadIdx.x >> 3, part = threadIdx.x & 7;
-    double c = 0.0;
+    float chi = 0.f, clo = 0.f;
     if (hh < nh) {
       const float* tot = blocktot + ((size_t)b * H + h0 + hh) * nT;
-      for (int kk = k + 1 + part; kk < nT; kk += 8) c += (double)tot[kk];
+      for (int kk0 = k + 1 + part; kk0 < nT; kk0 += 32) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = kk0 + 8 * q < nT ? tot[kk0 + 8 * q] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) two_sum_acc(chi, clo, v[q], 0.f);
+      }
     }
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (part == 0 && hh < nh) carry[hh] = (float)c;
+    for (int o = 4; o > 0; o >>= 1)
+      two_sum_acc(chi, clo, __shfl_xor_sync(0xffffffffu, chi, o), __shfl_xor_sync(0xffffffffu, clo, o));
+    if (part == 0 && hh < nh) carry[hh] = chi + clo;
   }
   {
     // R, C: thread e covers token e % 128 of head e / 128 (rows contiguous per head); loads first

@@ -36,12 +36,9 @@ namespace {
 
 
 // The fp32 dQ accumulator is blocked so that the 32 queries x 32 channels that one readout
-// warp adds at a time form one contiguous 4 KB block: [bh][Npad / 32][D / 32][32][32].
-template <int D>
-__device__ __forceinline__ size_t dq_offset(size_t bh, int Npad, int i, int e) {
-  return ((((bh * (size_t)(Npad >> 5) + (size_t)(i >> 5)) * (D / 32) + (size_t)(e >> 5)) << 10) +
-         (size_t)((i & 31) << 5) + (size_t)(e & 31));
-}
+// warp adds at a time form one contiguous 4 KB block: [bh][Npad / 32][D / 32][32][32]
+// (query i, channel e of (b, h) at block (bh (Npad / 32) + i / 32) (D / 32) + e / 32,
+// float (i % 32) 32 + e % 32 within it).
 
 // ------------------------------------------------------------------ rows
 // Delta_i = dO_i . O_i, the row offset rho_i and a cleared row sum for every row (b, i, h)
@@ -121,9 +118,6 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
     rho[r] = __int_as_float(0x7f800000);
   }
 }
-
-// Rows per warp of the dQ conversion.
-constexpr int kRowWarp = 4;
 
 // ------------------------------------------------------------------ main
 // One CTA per (b, h, 128-key tile J). The query tiles I >= J (every I when not
@@ -754,35 +748,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ out
-// One warp per kRowWarp consecutive rows (b, i, h), i < N; loads first, then the stores.
+// One warp per 4 KB block of the accumulator (32 queries x 32 channels of one (b, h)): the
+// block is read as eight contiguous 512-byte pieces, all issued first; each query's 32
+// channels go out as one 64-byte piece of its dQ row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Npad, float scale,
                                                     const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq) {
-  constexpr int E = D / 32;
-  using In = typename std::conditional<E == 4, float4, float2>::type;
-  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowWarp;
+  const long long blk = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const long long rows = (long long)B * N * H;
-  In v[kRowWarp];
+  const long long nblk = (long long)B * H * (Npad / 32) * (D / 32);
+  if (blk >= nblk) return;
+  const int cb = (int)(blk % (D / 32));           // channel block
+  const long long qbk = blk / (D / 32);
+  const int qblk = (int)(qbk % (Npad / 32));      // query block
+  const long long bh = qbk / (Npad / 32);
+  const int b = (int)(bh / H), h = (int)(bh % H);
+  const float4* src = reinterpret_cast<const float4*>(dqacc) + (size_t)blk * 256;  // 4 KB = 256 float4
+  float4 v[8];
 #pragma unroll
-  for (int r = 0; r < kRowWarp; ++r) {
-    const uint32_t row = static_cast<uint32_t>(row0 + r < rows ? row0 + r : rows - 1);  // B * N * H < 2^31
-    const uint32_t h = row % (uint32_t)H, bi = row / (uint32_t)H;
-    const uint32_t i = bi % (uint32_t)N, b = bi / (uint32_t)N;
-    v[r] = *reinterpret_cast<const In*>(dqacc + dq_offset<D>((size_t)b * H + h, Npad, i, lane * E));
-  }
+  for (int k = 0; k < 8; ++k) v[k] = src[k * 32 + lane];
 #pragma unroll
-  for (int r = 0; r < kRowWarp; ++r) {
-    if (row0 + r >= rows) break;
-    __nv_bfloat16* dst = dq + (size_t)(row0 + r) * D + lane * E;
-    if constexpr (E == 4) {
-      uint2 w;
-      w.x = pack_bf16x2(v[r].x * scale, v[r].y * scale);
-      w.y = pack_bf16x2(v[r].z * scale, v[r].w * scale);
-      *reinterpret_cast<uint2*>(dst) = w;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(v[r].x * scale, v[r].y * scale);
-    }
+  for (int k = 0; k < 8; ++k) {
+    const int q = 4 * k + (lane >> 3), i = qblk * 32 + q;  // query of this piece
+    if (i >= N) continue;
+    __nv_bfloat16* dst = dq + (((size_t)b * N + i) * H + h) * D + cb * 32 + (lane & 7) * 4;
+    uint2 w;
+    w.x = pack_bf16x2(v[k].x * scale, v[k].y * scale);
+    w.y = pack_bf16x2(v[k].z * scale, v[k].w * scale);
+    *reinterpret_cast<uint2*>(dst) = w;
   }
 }
 
@@ -974,11 +967,11 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long drows = (long long)a.B * a.N * a.H;
+  const long long dblocks = (long long)a.B * a.H * (g.Npad / 32) * (D / 32);  // 4 KB accumulator blocks
   {
     TraceScope trace("bwd_dq", s);
-    bwd_dq_kernel<D><<<(unsigned)((drows + 8 * kRowWarp - 1) / (8 * kRowWarp)), 256, 0, s>>>(a.B, a.N, a.H, g.Npad, a.scale, dqacc,
-                                                                   static_cast<__nv_bfloat16*>(a.dq));
+    bwd_dq_kernel<D><<<(unsigned)((dblocks + 7) / 8), 256, 0, s>>>(a.B, a.N, a.H, g.Npad, a.scale, dqacc,
+                                                                 static_cast<__nv_bfloat16*>(a.dq));
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

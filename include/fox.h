@@ -123,9 +123,10 @@ fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const v
 /*
  * Backward (bf16 only). Reads q, k, v, z, the forward's O and LSE, and the
  * upstream gradient dO; writes dq, dk, dv [B,N,H,d] bf16 and dz [B,N,H] fp32.
- * Steps: gate scan, Delta_i = dO_i . O_i, the fused recompute-and-backward
- * attention kernel (dK, dV, dQ accumulator and the column sums of dS), the
- * dQ conversion and the reverse gate scan. With non_causal = 1, Delta is not
+ * Steps: gate scan, the fp32 dQ accumulator in the workspace cleared (a
+ * stream-ordered cudaMemsetAsync), Delta_i = dO_i . O_i, the fused
+ * recompute-and-backward attention kernel (dK, dV, dQ accumulator and the
+ * column sums of dS), the dQ conversion and the reverse gate scan. With non_causal = 1, Delta is not
  * taken from the bf16 O: the forward kernel runs once more in a mode whose
  * P V product carries P as two bf16 terms and which writes dO_i . O_i from the
  * fp32 accumulator (the gate gradient is a small difference of large sums of

@@ -334,32 +334,27 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   if (p->non_causal) {
     // Without the causal mask the gate gradient is a small difference of large
     // row and column sums of dS = P (dP - Delta), and a Delta_i = dO_i . O_i
-    // taken from the bf16 O (or from an O built with bf16 P) moves it by
-    // several percent. Re-run the forward once in its Delta mode: P enters the
-    // P V product as two bf16 terms, and Delta comes from the fp32 accumulator;
-    // O and LSE are not written.
-    CUtensorMap fmaps[3];
-    if (!make_bnhd_map(&fmaps[0], q, p->B, p->N, p->H, p->d)) return FOX_ERR_CUDA;
-    fmaps[1] = maps[1];
-    fmaps[2] = maps[2];
-    AttnFwdArgs f;
-    f.B = p->B;
-    f.N = p->N;
-    f.H = p->H;
-    f.d = p->d;
-    f.scale = a.scale;
-    f.non_causal = 1;
-    f.q = q;
-    f.k = k;
-    f.v = v;
-    f.o = nullptr;
-    f.lse = nullptr;
-    f.rowloc = reinterpret_cast<const float*>(a.ws + g.rowloc);
-    f.colrec = reinterpret_cast<const float*>(a.ws + g.colrec);
-    f.err = reinterpret_cast<uint32_t*>(a.ws);
-    f.dO_for_delta = dO;
-    f.delta_out = reinterpret_cast<float*>(a.ws + w.delta);
-    if (launch_attn_fwd_bf16(f, fmaps, g.nT, g.Npad, s) != cudaSuccess) return FOX_ERR_CUDA;
+    // taken from the bf16 O moves it by several percent. Form Delta_i as
+    // sum_j P_ij dP_ij instead, from S = Q K^T and dP = dO V^T with P recomputed
+    // from LSE, all in fp32 (O is not read).
+    CUtensorMap dmaps[4];
+    if (!make_bnhd_map(&dmaps[0], q, p->B, p->N, p->H, p->d) ||
+        !make_bnhd_map(&dmaps[3], dO, p->B, p->N, p->H, p->d))
+      return FOX_ERR_CUDA;
+    dmaps[1] = maps[1];
+    dmaps[2] = maps[2];
+    DeltaArgs da;
+    da.B = p->B;
+    da.N = p->N;
+    da.H = p->H;
+    da.d = p->d;
+    da.scale = a.scale;
+    da.rowloc = reinterpret_cast<const float*>(a.ws + g.rowloc);
+    da.colrec = reinterpret_cast<const float*>(a.ws + g.colrec);
+    da.lse = lse;
+    da.delta = reinterpret_cast<float*>(a.ws + w.delta);
+    da.err = reinterpret_cast<uint32_t*>(a.ws);
+    if (launch_delta_pass(da, dmaps, g.nT, g.Npad, s) != cudaSuccess) return FOX_ERR_CUDA;
     a.delta_ready = 1;
   }
   return launch_attn_bwd(a, g, w, maps, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;

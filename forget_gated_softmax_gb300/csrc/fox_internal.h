@@ -159,6 +159,21 @@ struct AttnBwdArgs {
   const int* imax = nullptr;  // tile skipping: last query tile of each key tile ([bh][nT]), or null
 };
 
+// Delta_i = dO_i . O_i = sum_j P_ij dP_ij for every query row of the non-causal backward,
+// from S = Q K^T and dP = dO V^T on the tensor core and P recomputed from the forward's LSE
+// (no O needed): writes delta[bh][i] for i < N (layout [BH][Npad]).
+struct DeltaArgs {
+  int B, N, H, d;
+  float scale;
+  const float* rowloc;
+  const float* colrec;
+  const float* lse;
+  float* delta;
+  uint32_t* err;
+};
+cudaError_t launch_delta_pass(const DeltaArgs& a, const CUtensorMap* maps /* q, k, v, dO (128-row boxes) */, int nT,
+                              int Npad, cudaStream_t s);
+
 // Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ
 // conversion and the reverse gate scan; the gate scan must already be in ws.
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w,

@@ -505,8 +505,8 @@ def run_fox(args, rank: int, world: int, local_rank: int):
 
     nc_flops = 2 * (w.fwd_flops() + w.bwd_flops())  # the full N^2 score matrix instead of its causal half
     extra["non_causal"] = timed_variant(fox, torch, stream, nc_step, 5, nc_flops)
-    extra["non_causal"]["note"] = ("flops: 4BHN^2d forward + 10BHN^2d backward; the backward also re-runs the "
-                                   "forward once with a two-term P to form Delta")
+    extra["non_causal"]["note"] = ("flops: 4BHN^2d forward + 10BHN^2d backward; the backward first forms "
+                                   "Delta = sum_j P dP from S = Q K^T and dP = dO V^T (one forward's worth of MMAs)")
     assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
 
     # Gate projection fused with the gate scan (z = x W_f^T + b_f, hidden = H d): HBM-bound

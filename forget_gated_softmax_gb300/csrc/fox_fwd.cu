@@ -29,10 +29,6 @@
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
 // P (bf16) overwrites the first 64 columns of its S buffer and feeds the P V
 // MMA straight from tensor memory.
-//
-// Delta mode (kDelta, for the non-causal backward): P is written as two bf16
-// terms over all 128 columns and both feed the P V product, so O is accurate
-// to fp32 rounding; the epilogue writes dO_i . O_i per row instead of O and LSE.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -56,11 +52,6 @@ struct FwdKParams {
   float* lse;
   uint32_t* err;
   const int* jmin;  // tile skipping: first key tile of each query tile ([bh][nT]), or null
-  // Delta mode (used by the non-causal backward): instead of O and LSE, write
-  // delta[bh][i] = dO_i . O_i with O_i from the fp32 accumulator of a P V
-  // product whose P is split into two bf16 terms.
-  const __nv_bfloat16* dO;
-  float* delta;
 };
 
 template <int D>
@@ -126,34 +117,10 @@ __device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float sc
   return -mn;
 }
 
-// Upper bound of this row's t_j = scale2 * S_j - kappa_j over a tile without
-// masking: the column term is non-increasing along the tile (log f <= 0), so
-// max_j t_j <= scale2 * max_j S_j - kappa_127. Costs one FMNMX per element.
-__device__ __forceinline__ float row_bound(uint32_t tS, float scale2, float kappa_last) {
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-  for (int qt = 0; qt < 4; ++qt) {
-    uint32_t raw[32];
-    tmem_ld32(tS + 32 * qt, raw);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      m0 = fmaxf(m0, __uint_as_float(raw[j]));
-      m1 = fmaxf(m1, __uint_as_float(raw[j + 1]));
-      m2 = fmaxf(m2, __uint_as_float(raw[j + 2]));
-      m3 = fmaxf(m3, __uint_as_float(raw[j + 3]));
-    }
-  }
-  return fmaf(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)), scale2, -kappa_last);
-}
-
 // p_j = 2^(t_j - off) for the 128 columns, written back as bf16 pairs into
 // the first 64 columns of the same S row (chunk q's P lands on columns
 // [16q, 16q+16), which only hold S values already read). Returns sum_j p_j (fp32).
-// kSplit: p = hi + lo with hi = bf16(p), lo = bf16(p - hi) (about 16 significant
-// bits together); chunk q's hi goes to columns [32q, 32q+16) and lo to
-// [32q+16, 32q+32), the chunk's own columns, and both feed the P V product.
-template <bool kDiag, bool kSplit = false>
+template <bool kDiag>
 __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float scale2, float off, int r) {
   const float2 nsc = make_float2(-scale2, -scale2), noff = make_float2(-off, -off);
   float2 s = make_float2(0.f, 0.f);  // sums of the even and odd columns
@@ -163,7 +130,6 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
     tmem_ld32(tS + 32 * qt, raw);
     tmem_ld_wait();
     uint32_t pk[16];
-    uint32_t lo[kSplit ? 16 : 1];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;
@@ -187,20 +153,8 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
       s = fadd2(s, fadd2(make_float2(pr[0], pr[1]), make_float2(pr[2], pr[3])));
       pk[2 * j4] = pack_bf16x2(pr[0], pr[1]);
       pk[2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
-      if (kSplit) {
-        // The low halves of the packed pairs hold the even columns.
-        lo[2 * j4] = pack_bf16x2(pr[0] - __uint_as_float(pk[2 * j4] << 16),
-                                 pr[1] - __uint_as_float(pk[2 * j4] & 0xffff0000u));
-        lo[2 * j4 + 1] = pack_bf16x2(pr[2] - __uint_as_float(pk[2 * j4 + 1] << 16),
-                                     pr[3] - __uint_as_float(pk[2 * j4 + 1] & 0xffff0000u));
-      }
     }
-    if (kSplit) {
-      tmem_st16(tS + 32 * qt, pk);
-      tmem_st16(tS + 32 * qt + 16, lo);
-    } else {
-      tmem_st16(tS + 16 * qt, pk);
-    }
+    tmem_st16(tS + 16 * qt, pk);
   }
   return s.x + s.y;
 }
@@ -250,7 +204,7 @@ struct StageC {
   static constexpr int value = V;
 };
 
-template <int D, bool kDelta>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const FwdKParams p) {
@@ -391,24 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t dv = st ? dVs[1][ks] : dVs[0][ks];
-          if (kDelta) {  // P = hi + lo: chunk ks/2 holds hi at +0 and lo at +16 columns
-            const uint32_t a = tS[k] + 32 * (ks >> 1) + 8 * (ks & 1);
-            umma_ts(tO[k], a, dv, idO, (acc || ks > 0) ? 1u : 0u);
-            umma_ts(tO[k], a + 16, dv, idO, 1u);
-          } else {
-            umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
-          }
+          umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
         }
       };
       // One K-step of P V for Q tile k with the V descriptor dv.
       auto pv_ks = [&](int k, int ks, bool acc, uint64_t dv) {
-        if (kDelta) {  // P = hi + lo: chunk ks/2 holds hi at +0 and lo at +16 columns
-          const uint32_t a = tS[k] + 32 * (ks >> 1) + 8 * (ks & 1);
-          umma_ts(tO[k], a, dv, idO, (acc || ks > 0) ? 1u : 0u);
-          umma_ts(tO[k], a + 16, dv, idO, 1u);
-        } else {
-          umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
-        }
+        umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
                 mbar_wait(&bars[B_KFULL + 0], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
@@ -526,10 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float beta0 = (baseI_hi - kap[kTile]) + (baseI_lo - kap[kTile + 1]);
         if (causal) {
           m_used = row_max<true>(tS, kap, p.scale2, r);
-          l_sum = exp_pass<true, kDelta>(tS, kap, p.scale2, m_used, r);
+          l_sum = exp_pass<true>(tS, kap, p.scale2, m_used, r);
         } else {
           m_used = row_max<false>(tS, kap, p.scale2, r) + beta0;
-          l_sum = exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta0, r);
+          l_sum = exp_pass<false>(tS, kap, p.scale2, m_used - beta0, r);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -563,34 +505,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (grow) m_used = m_cand;
         };
-        if constexpr (kDelta) {
-          // Cheap bound first; the exact row maximum only when the bound says the running
-          // maximum might be exceeded by more than the threshold (rare: the first tile
-          // holds the largest bias).
-          const float bound = row_bound(tS, p.scale2, kap[kTile - 1]) + beta;
-          float m_cand = bound;
-          bool grow = false;
-          if (__any_sync(0xffffffffu, bound > m_used + kRescaleThreshold)) {
-            m_cand = row_max<false>(tS, kap, p.scale2, r) + beta;
-            grow = m_cand > m_used + kRescaleThreshold;
-          }
-          if (__any_sync(0xffffffffu, grow)) rescale(m_cand, grow);
-          l_sum += exp_pass<false, kDelta>(tS, kap, p.scale2, m_used - beta, r);
+        // One pass with the running maximum; the exact row maximum comes with it.
+        uint32_t pk[64];
+        float tmax;
+        const float lsum_tile = exp_pass_deferred(tS, kap, p.scale2, m_used - beta, pk, tmax);
+        const float m_cand = tmax + beta;
+        const bool grow = m_cand > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {  // rare: redo the tile with the new maximum
+          rescale(m_cand, grow);
+          l_sum += exp_pass<false>(tS, kap, p.scale2, m_used - beta, r);
         } else {
-          // One pass with the running maximum; the exact row maximum comes with it.
-          uint32_t pk[64];
-          float tmax;
-          const float lsum_tile = exp_pass_deferred(tS, kap, p.scale2, m_used - beta, pk, tmax);
-          const float m_cand = tmax + beta;
-          const bool grow = m_cand > m_used + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, grow)) {  // rare: redo the tile with the new maximum
-            rescale(m_cand, grow);
-            l_sum += exp_pass<false, false>(tS, kap, p.scale2, m_used - beta, r);
-          } else {
-            l_sum += lsum_tile;
-            tmem_st32(tS, pk);
-            tmem_st32(tS + 32, pk + 32);
-          }
+          l_sum += lsum_tile;
+          tmem_st32(tS, pk);
+          tmem_st32(tS + 32, pk + 32);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -599,31 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) ok = mbar_wait(&bars[B_OFINAL + k], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
       ok = __all_sync(0xffffffffu, ok);
-      if (kDelta && ok) {
-        tc_fence_after();
-        const float inv = 1.f / l_sum;
-        float dot = 0.f;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c, o);
-          tmem_ld_wait();
-          if (i < p.N) {
-            const uint4* g = reinterpret_cast<const uint4*>(p.dO + (((size_t)b * p.N + i) * p.H + h) * D + c);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const uint4 w = g[q4];
-              const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                dot = fmaf(__uint_as_float(wv[e] << 16), __uint_as_float(o[8 * q4 + 2 * e]), dot);
-                dot = fmaf(__uint_as_float(wv[e] & 0xffff0000u), __uint_as_float(o[8 * q4 + 2 * e + 1]), dot);
-              }
-            }
-          }
-        }
-        if (i < p.N) p.delta[(size_t)bh * p.Npad + i] = dot * inv;
-      } else if (!kDelta && ok) {
+      if (ok) {
         tc_fence_after();
         const float inv = 1.f / l_sum;
 #pragma unroll
@@ -661,8 +564,7 @@ template <int D>
 cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
   using L = FwdLayout<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  const bool delta = a.delta_out != nullptr;
-  auto kernel = delta ? fox_attn_fwd_kernel<D, true> : fox_attn_fwd_kernel<D, false>;
+  auto kernel = fox_attn_fwd_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdKParams p;
@@ -672,8 +574,6 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   p.nT = nT;
   p.nQB = (nT + 1) / 2;
   p.non_causal = a.non_causal;
-  p.dO = static_cast<const __nv_bfloat16*>(a.dO_for_delta);
-  p.delta = a.delta_out;
   p.Npad = Npad;
   p.scale2 = a.scale * kLog2e;
   p.rowloc = a.rowloc;
@@ -685,7 +585,7 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   const long long blocks = (long long)p.nQB * a.B * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
-    TraceScope trace(delta ? "attn_fwd_delta" : "attn_fwd", s);
+    TraceScope trace("attn_fwd", s);
     kernel<<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], p);
   }
   return cudaGetLastError();

@@ -127,10 +127,6 @@ struct AttnFwdArgs {
   const float* colrec;
   uint32_t* err;
   const int* jmin = nullptr;  // tile skipping: first key tile of each query tile ([bh][nT]), or null
-  // When delta_out is set, the kernel writes delta_out[bh][i] = dO_i . O_i (O in fp32)
-  // instead of O and LSE (rows i < N; layout [BH][Npad]).
-  const void* dO_for_delta = nullptr;
-  float* delta_out = nullptr;
 };
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v */, int nT, int Npad,
@@ -153,8 +149,8 @@ struct AttnBwdArgs {
   void* dv;
   float* dz;
   char* ws;  // workspace base (gate layout, then the backward layout)
-  // Set when Delta of rows i < N is already in the backward layout (the forward
-  // kernel's Delta epilogue wrote it); the row kernel then only writes the padding.
+  // Set when Delta of rows i < N is already in the backward layout (the non-causal
+  // backward's Delta pass wrote it); the row kernel then only writes the padding.
   int delta_ready = 0;
   const int* imax = nullptr;  // tile skipping: last query tile of each key tile ([bh][nT]), or null
 };

@@ -126,12 +126,12 @@ fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const v
  * Steps: gate scan, the fp32 dQ accumulator in the workspace cleared (a
  * stream-ordered cudaMemsetAsync), Delta_i = dO_i . O_i, the fused
  * recompute-and-backward attention kernel (dK, dV, dQ accumulator and the
- * column sums of dS), the dQ conversion and the reverse gate scan. With non_causal = 1, Delta is not
- * taken from the bf16 O: the forward kernel runs once more in a mode whose
- * P V product carries P as two bf16 terms and which writes dO_i . O_i from the
- * fp32 accumulator (the gate gradient is a small difference of large sums of
- * dS there, and the bf16 rounding of O moves it by percents). O still must
- * be the forward's output; the extra pass costs about 1.5 forwards.
+ * column sums of dS), the dQ conversion and the reverse gate scan.
+ * With non_causal = 1, Delta is not taken from the bf16 O: a pass of its own
+ * forms Delta_i = sum_j P_ij dP_ij from S = Q K^T and dP = dO V^T with P
+ * recomputed from LSE, in fp32 (the gate gradient is a small difference of
+ * large sums of dS there, and the bf16 rounding of O moves it by percents).
+ * The extra pass costs about one forward.
  */
 fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,
                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dz, void* workspace,

@@ -81,9 +81,10 @@ __global__ void __launch_bounds__(kDeltaThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int I = static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // Head-major order: the CTAs resident at once share one or two heads, whose K and V
+  // then stay in L2 across their query tiles.
+  const int I = static_cast<int>(blockIdx.x) % p.nT;
+  const int bh = static_cast<int>(blockIdx.x) / p.nT;
   const int b = bh / p.H, h = bh % p.H;
   const int nJ = p.nT;
 

@@ -80,12 +80,20 @@ def _code_only(src: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments and layout ignored); an ncu traffic figure is
-    only reported for the code it was taken on."""
+# Sources that determine each traced kernel's code and launch (its own translation unit, the
+# shared headers, and the host code that builds its tensor maps).
+KERNEL_SOURCES = {
+    "attn_fwd": ("fox_fwd.cu", "fox_api.cu", "fox_internal.h", "fox_ptx.cuh"),
+    "attn_bwd": ("fox_bwd.cu", "fox_api.cu", "fox_internal.h", "fox_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (comments and layout ignored) of the sources behind `kernel`; an ncu
+    traffic figure is only reported for the code it was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "forget_gated_softmax_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES.get(kernel, tuple(sorted(os.listdir(csrc)))):
         if f.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(_code_only(fh.read()).encode())
@@ -97,7 +105,7 @@ def ncu_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     pat = re.compile(r"^\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]+)\s*\|")
     with open(path) as f:
         for line in f:

@@ -286,6 +286,9 @@ def fox_fwd_noalloc(q, k, v, z, *, scale: float = 0.0, bias_from_j: bool = False
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, N, H), dtype=torch.float32, device=q.device)
+    for t in (q, k, v, z, o, lse):
+        if not t.is_contiguous():
+            raise ValueError("fox_fwd_noalloc needs contiguous tensors")
     st = lib().fox_fwd_noalloc(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(o), _ptr(lse),
                                _stream_handle(stream))
     if st != 0:

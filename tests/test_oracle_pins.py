@@ -421,6 +421,22 @@ def test_noncausal_rows_variant_matches_whole_head():
     np.testing.assert_allclose(lr, lse[rows], atol=1e-12)
 
 
+@pytest.mark.parametrize("from_j", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_delta_is_the_row_sum_of_p_times_dp(from_j, causal):
+    """Delta_i = dO_i . O_i equals sum_j P_ij dP_ij with dP_ij = dO_i . v_j (O_i = sum_j P_ij v_j):
+    the identity the non-causal backward's Delta pass uses to form Delta without O."""
+    N, d = 40, 8
+    q, k, v, z, dO = _rand_head(N, d, gate_mu=0.5, gate_sigma=1.5, seed=66)
+    O, _, P = ora.attention_head(q, k, v, z, bias_from_j=from_j, return_p=True, causal=causal)
+    delta_from_o = (dO * O).sum(axis=1)
+    delta_from_p = (P * (dO @ v.T)).sum(axis=1)
+    np.testing.assert_allclose(delta_from_p, delta_from_o, rtol=0, atol=1e-12)
+    # and dS = P (dP - Delta) has zero row sums with it (row-shift invariance of the softmax)
+    dS = P * ((dO @ v.T) - delta_from_p[:, None])
+    np.testing.assert_allclose(dS.sum(axis=1), 0.0, atol=1e-12)
+
+
 # ----------------------------------------------------------------- gate projection
 def test_gate_projection_is_torch_linear():
     """z = f_proj(x) with f_proj = nn.Linear(hidden, H, bias=True): the library routine in fp64."""

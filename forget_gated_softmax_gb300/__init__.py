@@ -43,6 +43,8 @@ EXPORTS = (
     "fox_trace_begin",
     "fox_trace_end",
     "fox_fwd_noalloc",
+    "fox_noalloc_check_error",
+    "fox_selftest_wait_timeout",
     "fox_noalloc_scratch_bytes",
     "fox_window",
     "fox_window_workspace_bytes",
@@ -123,6 +125,10 @@ def lib() -> ctypes.CDLL:
         L.fox_fwd_noalloc.restype = i
         L.fox_noalloc_scratch_bytes.argtypes = []
         L.fox_noalloc_scratch_bytes.restype = sz
+        L.fox_noalloc_check_error.argtypes = [vp]
+        L.fox_noalloc_check_error.restype = i
+        L.fox_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp, sz, vp]
+        L.fox_selftest_wait_timeout.restype = i
         L.fox_gate_scan_workspace_bytes.argtypes = [pp]
         L.fox_gate_scan_workspace_bytes.restype = sz
         L.fox_gate_scan.argtypes = [pp, vp, vp, vp, sz, vp]
@@ -435,6 +441,19 @@ def fox_tile_span(q, k, z, *, scale: float = 0.0, bias_from_j: bool = False, ws=
 def fox_check_error(ws, stream=None) -> int:
     """Synchronise and read (then clear) the workspace's device error word; returns the status."""
     return int(lib().fox_check_error(_ptr(ws), _stream_handle(stream)))
+
+
+def fox_noalloc_check_error(stream=None) -> int:
+    """fox_check_error for the fixed scratch of fox_fwd_noalloc on the current device."""
+    return int(lib().fox_noalloc_check_error(_stream_handle(stream)))
+
+
+def fox_selftest_wait_timeout(limit_us: int, ws, stream=None) -> None:
+    """Enqueue the device error path's self-test (a bounded wait that runs out; see
+    fox_selftest_wait_timeout in include/fox.h); read the outcome with fox_check_error(ws)."""
+    st = lib().fox_selftest_wait_timeout(int(limit_us), _ptr(ws), ws.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FoxError(st, "fox_selftest_wait_timeout")
 
 
 def trace_begin() -> None:

@@ -14,7 +14,10 @@
 // device current, on the first call made on it; that first call should come
 // before any stream capture. Every call shares the one array: the scratch is
 // fully rewritten by each call (its error word is cleared by the first kernel),
-// and calls whose work overlaps on the GPU race on it.
+// and calls whose work overlaps on the GPU race on it. fox_noalloc_check_error
+// reads the array's error word. The cached address lives as long as the process:
+// after a cudaDeviceReset the array is gone with the context, and this entry
+// point must not be used on that device again.
 #include <cstdint>
 #include <mutex>
 
@@ -55,6 +58,13 @@ cudaError_t scratch_for_current_device(void** out) {
 extern "C" {
 
 size_t fox_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
+
+// The scratch array's error word, read and cleared like any workspace's.
+fox_status fox_noalloc_check_error(void* stream) {
+  void* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return FOX_ERR_CUDA;
+  return fox_check_error(scratch, stream);
+}
 
 fox_status fox_fwd_noalloc(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
                            float* lse, void* stream) {

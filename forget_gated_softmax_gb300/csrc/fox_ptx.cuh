@@ -66,21 +66,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on the phase with the given parity. `abort_flag` (shared
 // memory) lets one role that already gave up release every other role at
 // once; `err` is the global error word. Returns false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err, uint32_t code) {
+// The limit is `limit_ns` of %globaltimer time.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* err, uint32_t code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > FOX_WAIT_TIMEOUT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         if (err) atomicOr(err, code);
         return false;
       }
     }
   }
+}
+
+// The same wait with the library's limit, FOX_WAIT_TIMEOUT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* err, uint32_t code) {
+  return mbar_wait_for(bar, parity, abort_flag, err, code, FOX_WAIT_TIMEOUT_NS);
 }
 
 // Wait bounded by time only (ignores the abort flag): used at teardown to let

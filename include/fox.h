@@ -225,11 +225,21 @@ fox_status fox_tile_span(const fox_params* p, const void* q, const void* k, cons
  * device current; make that first call before any stream capture. All calls
  * share the one array and the last call's contents stay in it: each call
  * rewrites it completely (the error word included), and calls whose work
- * overlaps on the GPU race on it. fox_check_error does not apply to it.
+ * overlaps on the GPU race on it. The device address is cached per device for
+ * the life of the process: a cudaDeviceReset() on a device destroys the array
+ * with the context, and fox_fwd_noalloc must not be called on that device
+ * again in the same process.
  */
 fox_status fox_fwd_noalloc(const fox_params* p, const void* q, const void* k, const void* v, const float* z,
                            void* o, float* lse, void* stream);
 size_t fox_noalloc_scratch_bytes(void);
+/*
+ * fox_check_error for fox_fwd_noalloc: synchronises `stream`, reads and clears
+ * the error word of the fixed scratch array of the current device (the one the
+ * last fox_fwd_noalloc on that device used), with fox_check_error's results.
+ * Allocates nothing.
+ */
+fox_status fox_noalloc_check_error(void* stream);
 
 /*
  * Synchronises `stream`, reads and clears the device error word of
@@ -238,6 +248,21 @@ size_t fox_noalloc_scratch_bytes(void);
  * stream itself reports an error.
  */
 fox_status fox_check_error(void* workspace, void* stream);
+
+/*
+ * Self-test of the device-side error path (the pages have no counterpart: this
+ * checks the library's own failure reporting). One kernel on `stream` waits on
+ * an mbarrier that nothing arrives at, with the attention kernels' bounded-wait
+ * code and a limit of limit_us microseconds (1 .. 100000), while a second wait
+ * of 16x that limit must be released by the first one's abort flag. Afterwards
+ * the workspace's error word holds the timeout bit of the first wait only, so
+ * fox_check_error(workspace, stream) returns FOX_ERR_TIMEOUT and clears it; the
+ * next two 32-bit words of the header hold what each wait returned (0 = gave
+ * up). Nothing faults; the context stays usable. workspace: >= 256 bytes,
+ * 256-byte aligned (any fox_* workspace qualifies). Returns FOX_ERR_INVALID_ARG
+ * for a limit out of range.
+ */
+fox_status fox_selftest_wait_timeout(unsigned limit_us, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Kernel-level timing, for benchmarks. Between fox_trace_begin() and

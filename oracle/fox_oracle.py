@@ -32,7 +32,8 @@ fixed choice here):
   * The module adds 1e-6 inside the log. The formula in both pages has no such
     term; the oracle uses the exact log-sigmoid.
   * The scale multiplies q.k only, never D (module forward()).
-  * Always causal (the module's "decoder" mode); no dropout.
+  * Causal by default (the module's "decoder" mode); causal=False is its
+    "encoder" mode, where the same outer difference biases every key. No dropout.
   * LSE (not on the pages) is the natural-log normaliser of the biased,
     scaled scores, per row, layout [B, N, H].
   * z = +inf means f = 1 exactly (log f = 0).
@@ -51,8 +52,10 @@ __all__ = [
     "forget_bias",
     "attention_head",
     "attention_rows",
+    "attention_head_blocked",
     "forward",
     "backward_head",
+    "backward_head_blocked",
     "backward",
     "gate_grad_bruteforce",
     "gate_grad_from_sums",
@@ -185,6 +188,95 @@ def attention_rows(q, k, v, z, rows, scale=None, bias_from_j=False, causal=True)
         lse[n] = m + np.log(np.exp(s - m).sum())
         O[n] = np.exp(s - lse[n]) @ v[:last]
     return O, lse
+
+
+def _row_block_scores(q, k, c, col, r0, r1, scale, causal):
+    """S of query rows r0..r1-1 against the keys they see, as attention_head forms it:
+    scale * q_i . k_j + (c_i - colterm_j), with keys j > i set to -inf under the causal
+    mask [FoX-module, forward()]. Causal rows r0..r1-1 see keys 0..r1-1 only, so the
+    keys past r1 (all -inf for these rows) are left out. Returns (S, number of keys)."""
+    last = r1 if causal else k.shape[0]
+    S = scale * (q[r0:r1] @ k[:last].T) + (c[r0:r1, None] - col[None, :last])
+    if causal:
+        S[np.arange(r0, r1)[:, None] < np.arange(last)[None, :]] = -np.inf
+    return S, last
+
+
+def attention_head_blocked(q, k, v, z, scale=None, bias_from_j=False, causal=True, block=1024):
+    """attention_head's forward of one (b, h), evaluated one block of query rows at a time.
+
+    Row i of S (and so of P, O and LSE) depends only on q_i and the keys, so the
+    definition applied to rows r0..r1-1 alone gives exactly those rows. Memory is
+    O(block * N) instead of O(N^2): for sequences too long to hold S whole. The steps
+    per block are attention_head's: biased scaled logits, causal mask, LSE, P, P @ v.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    a = log_forget_gate(z)
+    c = cumulative_log_gate(a)
+    col = _column_term(c, a, bias_from_j)
+    O = np.empty((N, v.shape[1]))
+    lse = np.empty(N)
+    for r0 in range(0, N, block):
+        r1 = min(N, r0 + block)
+        S, last = _row_block_scores(q, k, c, col, r0, r1, scale, causal)
+        M = S.max(axis=1)
+        lse[r0:r1] = M + np.log(np.exp(S - M[:, None]).sum(axis=1))
+        O[r0:r1] = np.exp(S - lse[r0:r1, None]) @ v[:last]
+    return O, lse
+
+
+def backward_head_blocked(q, k, v, z, dO, scale=None, bias_from_j=False, causal=True, block=1024,
+                          return_sums=False):
+    """backward_head's gradients of one (b, h), one block of query rows at a time.
+
+    For rows r0..r1-1: S, LSE, P and O of those rows (attention_head_blocked), then the
+    same chain rule as backward_head restricted to them:
+      dP = dO_blk v^T,  Delta = rowsum(dO_blk * O_blk),  dS = P (dP - Delta),
+      dQ_blk = scale dS k;  dV += P^T dO_blk;  dK += scale dS^T q_blk;
+      R_blk = rowsum(dS);  C += colsum(dS).
+    Every dS_ij lands in exactly one block (its row's), so the sums over blocks are
+    backward_head's sums over i. The gate gradient is then gate_grad_from_sums(R, C, z).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    dO = np.asarray(dO, np.float64)
+    z = np.asarray(z, np.float64)
+    N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    a = log_forget_gate(z)
+    c = cumulative_log_gate(a)
+    col = _column_term(c, a, bias_from_j)
+    dQ = np.empty((N, d))
+    dK = np.zeros((N, d))
+    dV = np.zeros((N, v.shape[1]))
+    R = np.empty(N)
+    C = np.zeros(N)
+    for r0 in range(0, N, block):
+        r1 = min(N, r0 + block)
+        S, last = _row_block_scores(q, k, c, col, r0, r1, scale, causal)
+        M = S.max(axis=1)
+        lse = M + np.log(np.exp(S - M[:, None]).sum(axis=1))
+        P = np.exp(S - lse[:, None])
+        O = P @ v[:last]
+        dP = dO[r0:r1] @ v[:last].T
+        delta = (dO[r0:r1] * O).sum(axis=1)
+        dS = P * (dP - delta[:, None])
+        dQ[r0:r1] = scale * (dS @ k[:last])
+        dV[:last] += P.T @ dO[r0:r1]
+        dK[:last] += scale * (dS.T @ q[r0:r1])
+        R[r0:r1] = dS.sum(axis=1)
+        C[:last] += dS.sum(axis=0)
+    dz = gate_grad_from_sums(R, C, z, bias_from_j)
+    if return_sums:
+        return dQ, dK, dV, dz, {"R": R, "C": C}
+    return dQ, dK, dV, dz
 
 
 def forward(q, k, v, z, scale=None, bias_from_j=False, causal=True):

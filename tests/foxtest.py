@@ -22,17 +22,79 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return wl.bf16_bits_to_f64(wl.f32_to_bf16_bits(np.asarray(x, dtype=np.float32)))
 
 
-def o_excess_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype: str) -> float:
-    """max |O_gpu - O_ref| beyond the rounding of O_ref itself to the output format.
+def bf16_neighbours(x: np.ndarray):
+    """The bf16 values just below and just above each finite, nonzero fp64 x (both equal
+    to x when x is a bf16 value). bf16 keeps 8 significant bits: with x = m 2^e,
+    1/2 <= |m| < 1 (frexp), the spacing in x's binade is 2^(e-8), and x / 2^(e-8),
+    its floor and its ceiling are exact in fp64."""
+    x = np.asarray(x, np.float64)
+    _, e = np.frexp(x)
+    ulp = np.ldexp(1.0, e - 8)
+    return np.floor(x / ulp) * ulp, np.ceil(x / ulp) * ulp
 
-    A bf16 output cannot be closer to the exact value than bf16(O_ref) is; for
-    |O| in [4, 8) that rounding alone reaches 2^-6 = 0.0156 > 1e-2. So the
-    stated O tolerance bounds the error left after subtracting, element by
-    element, |bf16(O_ref) - O_ref| (zero for fp32 outputs)."""
+
+# Plain max |O_gpu - O_ref| of every forward comparison, for the end-of-session summary.
+PARITY_LOG = []
+
+
+def o_check(o_gpu: np.ndarray, o_ref: np.ndarray, dtype: str, label: str = "") -> dict:
+    """The O bound, element by element: max |O_gpu - O_ref| <= 1e-2 (bf16) or 1e-4 (fp32).
+
+    One exception for bf16 outputs: where |O_ref| >= 4 the bf16 spacing is 2^-5, so even
+    the correctly rounded value can sit up to 2^-6 = 0.0156 from O_ref. There O_gpu must
+    be one of the two bf16 neighbours of O_ref (the value rounded down or up). Returns the
+    plain max error over all elements, the max over |O_ref| < 4, the count of |O_ref| >= 4
+    elements and the count of elements failing the rule."""
+    o_gpu = np.asarray(o_gpu, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
     err = np.abs(o_gpu - o_ref)
+    tol = TOL_O_BF16 if dtype == "bf16" else TOL_O_F32
     if dtype == "bf16":
-        err = err - np.abs(bf16_round(o_ref) - o_ref)
-    return float(err.max()) if err.size else 0.0
+        big = np.abs(o_ref) >= 4.0
+        ok = err <= tol
+        if big.any():
+            lo, hi = bf16_neighbours(o_ref[big])
+            ok[big] = (o_gpu[big] == lo) | (o_gpu[big] == hi)
+    else:
+        big = np.zeros(err.shape, dtype=bool)
+        ok = err <= tol
+    res = {
+        "max_abs": float(err.max()) if err.size else 0.0,
+        "max_abs_below_4": float(err[~big].max()) if (~big).any() else 0.0,
+        "n_big": int(big.sum()),
+        "n_fail": int((~ok).sum()),
+        "finite": bool(np.isfinite(o_gpu).all()),
+    }
+    if label:
+        PARITY_LOG.append((label, res["max_abs"], res["n_big"]))
+    return res
+
+
+def assert_o(o_gpu, o_ref, dtype: str, label: str) -> dict:
+    res = o_check(o_gpu, o_ref, dtype, label)
+    assert res["finite"] and res["n_fail"] == 0, (label, res)
+    return res
+
+
+def map_heads(fn, items, threads: int = 0):
+    """fn over items in a thread pool (the oracle's numpy calls release the GIL), with the
+    BLAS pool held to one thread per call where threadpoolctl is available."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    threads = threads or min(16, os.cpu_count() or 1)
+    try:
+        from threadpoolctl import threadpool_limits
+
+        limit = threadpool_limits(1)
+    except ImportError:
+        limit = None
+    try:
+        with ThreadPoolExecutor(threads) as ex:
+            return list(ex.map(fn, items))
+    finally:
+        if limit is not None:
+            limit.restore_original_limits()
 
 
 def to_torch(arrays, dtype: str, device="cuda"):

@@ -111,6 +111,14 @@ def test_check_error_rejects_bad_workspace(L):
     assert L.fox_check_error(FAKE + 4, None) == 3
 
 
+def test_selftest_rejects_bad_arguments_on_host(L):
+    assert L.fox_selftest_wait_timeout(0, FAKE, 256, None) == 1
+    assert L.fox_selftest_wait_timeout(100001, FAKE, 256, None) == 1
+    assert L.fox_selftest_wait_timeout(1000, None, 256, None) == 3
+    assert L.fox_selftest_wait_timeout(1000, FAKE + 16, 256, None) == 3
+    assert L.fox_selftest_wait_timeout(1000, FAKE, 255, None) == 3
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fox, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(fox, "_lib", None)

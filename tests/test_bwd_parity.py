@@ -1,15 +1,18 @@
 """Backward parity: dQ, dK, dV and dz from the CUDA path (through the C ABI)
 against the CPU fp64 oracle's chain-rule gradients on the same seeded inputs.
 The bar is the relative Frobenius error ||g - g_ref|| / ||g_ref|| <= 2e-2 per
-gradient; small cases are compared whole, the full-size training workload on
-whole sampled heads (every (b, h) is independent)."""
+gradient; small cases are compared whole. The full-size shapes are compared on
+whole heads through the oracle's row-blocked backward, each head on its own
+(every (b, h) is independent): the long-context shape that the benchmark step
+times (B1 H32 N16384 d128) on heads 0, 1, 16 and 31 (fastest to slowest
+forgetting), and the training workload on 16 heads spread over all 8 batches."""
 import numpy as np
 import pytest
 
 import workloads as wl
 from oracle import fox_oracle as ora
 
-from foxtest import TOL_GRAD_REL, exact, tensor_f64, to_torch
+from foxtest import PARITY_LOG, TOL_GRAD_REL, exact, map_heads, tensor_f64, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +50,7 @@ def rel(g, r):
 
 
 def check_heads(w: wl.Workload, heads=None, scale=0.0, non_causal=False):
+    """The whole gradient tensors of the listed heads (default: all) against backward_head."""
     arrays, (dq, dk, dv, dz) = run_fwd_bwd(w, scale, non_causal=non_causal)
     for g in (dq, dk, dv, dz):
         assert np.isfinite(g).all()
@@ -64,6 +68,30 @@ def check_heads(w: wl.Workload, heads=None, scale=0.0, non_causal=False):
     for n, e in errs.items():
         assert e <= TOL_GRAD_REL, (w.name, n, e, errs)
     return errs
+
+
+def check_heads_blocked(w: wl.Workload, heads, arrays=None, non_causal=False, block=1024):
+    """Whole heads of a full-size shape, each against the row-blocked oracle backward, each
+    gradient of each head within the bar on its own; heads run in a thread pool."""
+    arrays, (dq, dk, dv, dz) = run_fwd_bwd(w, arrays=arrays, non_causal=non_causal)
+    for g in (dq, dk, dv, dz):
+        assert np.isfinite(g).all()
+    x = exact(arrays, "bf16")
+
+    def one(bh):
+        b, h = bh
+        return ora.backward_head_blocked(x["q"][b, :, h], x["k"][b, :, h], x["v"][b, :, h], x["z"][b, :, h],
+                                         x["dO"][b, :, h], bias_from_j=w.bias_from_j, causal=not non_causal,
+                                         block=block)
+
+    worst = {}
+    for (b, h), r in zip(heads, map_heads(one, heads, threads=min(8, len(heads)))):
+        errs = {n: rel(g[b, :, h], rr) for n, g, rr in zip(("dq", "dk", "dv", "dz"), (dq, dk, dv, dz), r)}
+        for n, e in errs.items():
+            worst[n] = max(worst.get(n, 0.0), e)
+            assert e <= TOL_GRAD_REL, (w.name, (b, h), n, e, errs)
+    PARITY_LOG.append((f"bwd {w.name}{' non-causal' if non_causal else ''} worst head rel", worst, len(heads)))
+    return worst
 
 
 SMALL = [
@@ -108,9 +136,18 @@ def test_open_gate_has_zero_gate_gradient():
     assert rel(dq[0, :, 0], r[0]) <= TOL_GRAD_REL and rel(dv[0, :, 0], r[2]) <= TOL_GRAD_REL
 
 
-def test_train_workload_sampled_heads():
-    w = wl.TRAIN_BF16
-    check_heads(w, heads=[(0, 0), (0, 15), (3, 7), (5, 2), (7, 15)])
+def test_long_shape_backward_heads():
+    """The backward the benchmark step times: B1 H32 N16384 d128, b_h = linspace(0, 8, 32),
+    dO ~ N(0, 1). Heads 0 and 1 forget fastest (a ~ -0.7 per token), 31 slowest; dz is a
+    suffix scan over all 16384 tokens."""
+    check_heads_blocked(wl.LONG_BF16, [(0, 0), (0, 1), (0, 16), (0, 31)], arrays=wl.draw(wl.LONG_BF16, with_dO=True))
+
+
+def test_train_workload_backward_16_heads():
+    """B8 H16 N4096 d128: two heads of every batch, 16 distinct heads in all."""
+    heads = [(b, h) for b in range(8) for h in ((2 * b) % 16, (2 * b + 9) % 16)]
+    assert len({h for _, h in heads}) == 16
+    check_heads_blocked(wl.TRAIN_BF16, heads, block=512)
 
 
 def test_backward_determinism():
@@ -122,6 +159,15 @@ def test_backward_determinism():
     for n in (1, 2):
         np.testing.assert_array_equal(g1[n], g2[n])
     assert rel(g1[0], g2[0]) < 1e-3 and rel(g1[3], g2[3]) < 1e-3
+
+
+@pytest.mark.parametrize("from_j", [False, True])
+def test_noncausal_backward_long(from_j):
+    """Encoder mode at N = 2048 (16 key tiles per query row), both conventions: the gate
+    gradient there is a small difference of large row and column sums over every key."""
+    w = wl.Workload(f"bnc_long_j{int(from_j)}", 1, 2048, 2, 128, "bf16", seed=2048 + int(from_j), gate="head_uniform",
+                    lo=1.0, hi=5.0, bias_from_j=from_j, backward=True)
+    check_heads_blocked(w, [(0, 0), (0, 1)], non_causal=True, block=512)
 
 
 @pytest.mark.parametrize("B,N,H,d", [(1, 5, 2, 128), (2, 129, 2, 64), (1, 300, 2, 128), (1, 640, 1, 64)])

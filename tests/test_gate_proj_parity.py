@@ -16,7 +16,7 @@ import pytest
 import workloads as wl
 from oracle import fox_oracle as ora
 
-from foxtest import TOL_LSE_BF16, TOL_O_BF16, exact, o_excess_error, sample_rows, tensor_f64, to_torch
+from foxtest import TOL_LSE_BF16, exact, assert_o, sample_rows, tensor_f64, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -96,7 +96,7 @@ def test_fwd_xgate_equals_fwd_on_projected_z(B, N, H, d, hidden, from_j):
     x = exact(arrays, "bf16")
     z_ref = ora.gate_projection(ex["x"], ex["w_f"], ex["b_f"])
     O_ref, L_ref = ora.forward(x["q"], x["k"], x["v"], z_ref, bias_from_j=from_j)
-    assert o_excess_error(tensor_f64(o1), O_ref, "bf16") <= TOL_O_BF16
+    assert_o(tensor_f64(o1), O_ref, "bf16", "xgate small")
     assert np.abs(tensor_f64(l1) - L_ref).max() <= TOL_LSE_BF16
 
 
@@ -119,7 +119,7 @@ def test_long_workload_xgate_sampled():
     for h in (0, 13, 31):
         rows = sample_rows(w.N, 10, h)
         Or, Lr = ora.attention_rows(x["q"][0, :, h], x["k"][0, :, h], x["v"][0, :, h], z_ref[:, h], rows)
-        assert o_excess_error(O[0, rows, h], Or, "bf16") <= TOL_O_BF16
+        assert_o(O[0, rows, h], Or, "bf16", "xgate long sampled rows")
         assert np.abs(L[0, rows, h] - Lr).max() <= TOL_LSE_BF16
 
 

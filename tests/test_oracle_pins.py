@@ -423,6 +423,54 @@ def test_noncausal_rows_variant_matches_whole_head():
 
 @pytest.mark.parametrize("from_j", [False, True])
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("block", [1, 64, 128, 1000])
+def test_row_blocked_forward_matches_whole_head(from_j, causal, block):
+    """The row-blocked forward (used where S does not fit whole) against the whole-head
+    definition: blocks of 1 row, ragged blocks and one block over everything."""
+    N, d = 300, 16
+    q, k, v, z, _ = _rand_head(N, d, gate_mu=0.5, gate_sigma=1.5, seed=71)
+    O, lse = ora.attention_head(q, k, v, z, scale=0.3, bias_from_j=from_j, causal=causal)
+    Ob, lb = ora.attention_head_blocked(q, k, v, z, scale=0.3, bias_from_j=from_j, causal=causal, block=block)
+    np.testing.assert_allclose(Ob, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lb, lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("from_j", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("block", [1, 64, 1000])
+def test_row_blocked_backward_matches_whole_head(from_j, causal, block):
+    """The row-blocked backward against backward_head (itself pinned to finite differences,
+    the double-sum gate gradient and autograd through SDPA): every gradient, and the row
+    and column sums of dS that the gate gradient is formed from."""
+    N, d = 300, 16
+    q, k, v, z, dO = _rand_head(N, d, gate_mu=0.5, gate_sigma=1.5, seed=72)
+    ref = ora.backward_head(q, k, v, z, dO, scale=0.3, bias_from_j=from_j, causal=causal, return_sums=True)
+    got = ora.backward_head_blocked(q, k, v, z, dO, scale=0.3, bias_from_j=from_j, causal=causal, block=block,
+                                    return_sums=True)
+    for n, r, g in zip(("dQ", "dK", "dV", "dz"), ref[:4], got[:4]):
+        np.testing.assert_allclose(g, r, rtol=0, atol=1e-11 * max(1.0, np.abs(r).max()), err_msg=n)
+    np.testing.assert_allclose(got[4]["R"], ref[4]["R"], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(got[4]["C"], ref[4]["C"], rtol=0, atol=1e-11)
+
+
+def test_row_blocked_open_gate_backward_matches_torch_autograd_sdpa():
+    """The row-blocked backward pinned directly to a library routine: with f = 1 it is
+    autograd through causal SDPA (dz = 0)."""
+    N, d = 200, 8
+    q, k, v, _, dO = _rand_head(N, d, seed=73)
+    z = np.full(N, np.inf)
+    dQ, dK, dV, dz = ora.backward_head_blocked(q, k, v, z, dO, block=48)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None], is_causal=True)[0]
+    out.backward(torch.tensor(dO))
+    np.testing.assert_allclose(dQ, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dK, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dV, tv.grad.numpy(), atol=1e-12)
+    np.testing.assert_array_equal(dz, 0.0)
+
+
+@pytest.mark.parametrize("from_j", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
 def test_delta_is_the_row_sum_of_p_times_dp(from_j, causal):
     """Delta_i = dO_i . O_i equals sum_j P_ij dP_ij with dP_ij = dO_i . v_j (O_i = sum_j P_ij v_j):
     the identity the non-causal backward's Delta pass uses to form Delta without O."""

@@ -21,14 +21,23 @@
 //
 // CTA = one (b, h) and a block of 256 query rows = two 128-row Q tiles that
 // share every K/V tile (ping-pong: while the softmax of one tile runs, the
-// tensor core works on the other). Warp roles (320 threads):
+// tensor core works on the other). Warp roles (384 threads):
 //   warps 0-3  softmax + epilogue of Q tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax + epilogue of Q tile 1
 //   warp  8    TMA producer (Q once; K, V and the column-term record per KV tile, 2 stages)
 //   warp  9    TMEM allocator and single-thread MMA issuer
+//   warps 10-11 V converters: each V tile from bf16 to fp16, in place in shared memory
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
-// P (bf16) overwrites the first 64 columns of its S buffer and feeds the P V
+// P (fp16) overwrites the first 64 columns of its S buffer and feeds the P V
 // MMA straight from tensor memory.
+//
+// P V runs in fp16 (P and V both fp16, fp32 accumulation). With bf16 P its
+// 8-bit significand adds up to about 2.5e-3 to O on these workloads, on top of
+// the up to 2^-7 of O's own bf16 rounding, which passes the 1e-2 bound on O; the
+// 11 bits of fp16 P leave only the output rounding. Every bf16 V value of
+// magnitude in [2^-14, 65280] is exactly an fp16 value, smaller ones round to
+// the nearest multiple of 2^-24, and a magnitude of 65536 or more (outside
+// fp16) sets DEV_ERR_RANGE in the error word.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +47,9 @@
 namespace fox {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 2;  // V converter warps (one measured 21 % slower on the long workload, three or
+                               // four 9-11 %: their threads lower the register cap of every warp to 128)
+constexpr int kThreads = 320 + 32 * kConvWarps;
 constexpr int kKappaBytes = kColRec * 4;   // 528
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum while the tile max stays within 2^8
 
@@ -63,7 +74,7 @@ struct FwdLayout {
   static constexpr int kV = 4 * kTileBytes;
   static constexpr int kKappa = 6 * kTileBytes;
   static constexpr int kBars = kKappa + 2 * kKappaBytes;  // 8-byte aligned (528 * 2 = 1056)
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // Slack for 1024-byte alignment of the base; at least 116 KB so that only one CTA (which
@@ -81,6 +92,7 @@ enum Bar {
   B_PFULL = 11,   // +tile (one arrival per softmax warp)
   B_OFINAL = 13,  // +tile
   B_DONE = 15,
+  B_VCONV = 16,   // +stage: the V tile of the stage converted to fp16 (one arrival per converter warp)
 };
 
 // Row maximum of t_j = scale2 * S_j - kappa_j over the 128 columns of this
@@ -117,7 +129,7 @@ __device__ __forceinline__ float row_max(uint32_t tS, const float* kap, float sc
   return -mn;
 }
 
-// p_j = 2^(t_j - off) for the 128 columns, written back as bf16 pairs into
+// p_j = 2^(t_j - off) for the 128 columns, written back as fp16 pairs into
 // the first 64 columns of the same S row (chunk q's P lands on columns
 // [16q, 16q+16), which only hold S values already read). Returns sum_j p_j (fp32).
 template <bool kDiag>
@@ -151,8 +163,8 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
       pr[2] = ex2_approx(wc.x);
       pr[3] = ex2_approx(wc.y);
       s = fadd2(s, fadd2(make_float2(pr[0], pr[1]), make_float2(pr[2], pr[3])));
-      pk[2 * j4] = pack_bf16x2(pr[0], pr[1]);
-      pk[2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
+      pk[2 * j4] = pack_f16x2(pr[0], pr[1]);
+      pk[2 * j4 + 1] = pack_f16x2(pr[2], pr[3]);
     }
     tmem_st16(tS + 16 * qt, pk);
   }
@@ -160,7 +172,7 @@ __device__ __forceinline__ float exp_pass(uint32_t tS, const float* kap, float s
 }
 
 // One pass over the row for the tiles after the first: p_j = 2^(t_j - off) into
-// registers (pk, packed bf16, not yet stored) together with max_j t_j (tmax), so
+// registers (pk, packed fp16, not yet stored) together with max_j t_j (tmax), so
 // that S is read from tensor memory once. The caller stores pk over the first 64
 // columns, or, in the rare case that the row maximum grew past the threshold,
 // discards it and recomputes P with the new maximum (S is still intact then).
@@ -190,8 +202,8 @@ __device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap
       pr[2] = ex2_approx(wc.x);
       pr[3] = ex2_approx(wc.y);
       s = fadd2(s, fadd2(make_float2(pr[0], pr[1]), make_float2(pr[2], pr[3])));
-      pk[16 * qt + 2 * j4] = pack_bf16x2(pr[0], pr[1]);
-      pk[16 * qt + 2 * j4 + 1] = pack_bf16x2(pr[2], pr[3]);
+      pk[16 * qt + 2 * j4] = pack_f16x2(pr[0], pr[1]);
+      pk[16 * qt + 2 * j4 + 1] = pack_f16x2(pr[2], pr[3]);
     }
   }
   tmax = -mn;
@@ -248,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_SFULL + s], 1);
       mbar_init(&bars[B_PFULL + s], 4);
       mbar_init(&bars[B_OFINAL + s], 1);
+      mbar_init(&bars[B_VCONV + s], kConvWarps);
     }
     mbar_init(&bars[B_DONE], 1);
     *abort_flag = 0;
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t tb = L::kTileBytes;
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idO = idesc_f16(128, D, false, true);  // P (TMEM) and V fp16
       const uint32_t tS[2] = {tbase, tbase + 128};
       const uint32_t tO[2] = {tbase + 256, tbase + 256 + D};
       // Descriptors of each operand tile's base. Shared-memory addresses stay below 2^18, so
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // on the stage parity so that every descriptor and barrier address is fixed.
         auto straight = [&](auto stage) -> bool {
           constexpr int ST = decltype(stage)::value, NST = ST ^ 1;
-          bool ok = mbar_wait(&bars[B_VFULL + ST], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
+          bool ok = mbar_wait(&bars[B_VCONV + ST], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC) &&
                     mbar_wait(&bars[B_PFULL + 0], (s - first0) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) return false;
           tc_fence_after();
@@ -396,10 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) pv_ks(1, ks, s > 0, dVs[ST][ks]);
+          // The V stage is free once the last P V reading it retires: released before the next
+          // S group so that the following V load (and its conversion) starts earlier.
+          umma_commit(&bars[B_VEMPTY + ST]);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[1], dA[1][ks], dB[NST][ks], idS, ks > 0);
           umma_commit(&bars[B_SFULL + 1]);
-          umma_commit(&bars[B_VEMPTY + ST]);
           umma_commit(&bars[B_KEMPTY + NST]);
           return true;
         };
@@ -408,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           continue;
         }
-        ok = mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
+        ok = mbar_wait(&bars[B_VCONV + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
         for (int k = 0; k < 2 && ok; ++k) {
           if (!active[k]) continue;
           if (s >= first[k] && s < end[k]) {
@@ -438,6 +453,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bars[B_DONE], 0);
     }
     __syncwarp();
+  } else if (warp >= 10) {
+    // ----------------------------------------------------------- V converters
+    // Each V tile in place from bf16 to fp16, the two warps taking alternate 16-byte pieces
+    // of the swizzled layout TMA wrote (the conversion is per element, so the layout is
+    // unchanged), then a proxy fence so that the MMA's reads see the generic-proxy stores.
+    uint32_t vmax = 0u;  // largest |v| bit pattern seen, per bf16 half
+    for (int s = 0; s < nJ; ++s) {
+      const int st = s & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL + st], (s >> 1) & 1, abort_flag, p.err,
+                                                         DEV_ERR_TIMEOUT_TMA));
+      if (!ok) break;
+      uint4* tile = reinterpret_cast<uint4*>(sm + L::kV + st * L::kTileBytes);
+#pragma unroll 4
+      for (int e = (warp - 10) * 32 + lane; e < L::kTileBytes / 16; e += 32 * kConvWarps) {
+        const uint4 w = tile[e];
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          out[c] = pack_f16x2(__uint_as_float(in[c] << 16), __uint_as_float(in[c] & 0xFFFF0000u));
+          asm("max.u16x2 %0, %0, %1;" : "+r"(vmax) : "r"(in[c] & 0x7FFF7FFFu));
+        }
+        tile[e] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_VCONV + st]);
+    }
+    // |v| >= 65536 (bf16 pattern 0x4780 and above, infinities included) is outside fp16.
+    const bool over = (vmax & 0xFFFFu) >= 0x4780u || (vmax >> 16) >= 0x4780u;
+    if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(p.err, DEV_ERR_RANGE);
   } else {
     // ------------------------------------------------------ softmax / epilogue
     const int k = warp >> 2;        // Q tile of this warpgroup

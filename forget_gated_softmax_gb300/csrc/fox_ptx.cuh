@@ -21,6 +21,7 @@ enum : uint32_t {
   DEV_ERR_TIMEOUT_MMA = 1u << 1,   // a wait for a tensor-core commit gave up
   DEV_ERR_TIMEOUT_SYNC = 1u << 2,  // a wait between warp roles gave up
   DEV_ERR_BOUNDS = 1u << 3,        // a debug bounds check caught an index
+  DEV_ERR_RANGE = 1u << 4,         // an input value outside the range a kernel's arithmetic format holds
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -249,6 +250,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with fp16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)  // D format: f32 (A and B format fields 0: f16)
+         | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // TMEM loads/stores: warp w reaches lanes [32*(w%4), 32*(w%4)+32); thread t
 // gets/puts N consecutive 32-bit columns of lane 32*(w%4)+t.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
@@ -302,6 +310,13 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Pack two fp32 into f16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

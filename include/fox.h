@@ -57,7 +57,8 @@ typedef enum fox_status {
   FOX_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than the size query */
   FOX_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   FOX_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (from fox_check_error) */
-  FOX_ERR_DEVICE = 6       /* another device-side error bit was set (from fox_check_error) */
+  FOX_ERR_DEVICE = 6       /* another device-side error bit was set (from fox_check_error), e.g. a
+                              V value outside the fp16 range of the forward's P V product */
 } fox_status;
 
 enum { FOX_DTYPE_BF16 = 0, FOX_DTYPE_F32 = 1 };
@@ -91,6 +92,12 @@ size_t fox_bwd_workspace_bytes(const fox_params* p);
  * LSE [B,N,H] (fp32, natural log, bias included).
  * Steps: gate log-sigmoid + per-head prefix scan into the workspace, then the
  * fused causal attention kernel. B*H == 0 or N == 0 returns FOX_OK with no work.
+ * Precision (bf16): S = Q K^T in bf16 with fp32 accumulation, the softmax in
+ * fp32, and P V in fp16 (P and V converted to fp16 on chip, fp32 accumulation),
+ * so that the weights carry 11 significant bits instead of bf16's 8. Every bf16
+ * V value of magnitude 2^-14 .. 65280 converts exactly; smaller ones round to a
+ * multiple of 2^-24; a V value of magnitude 65536 or more sets a device error
+ * bit (fox_check_error then returns FOX_ERR_DEVICE).
  */
 fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
                    float* lse, void* workspace, size_t workspace_bytes, void* stream);

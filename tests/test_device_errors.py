@@ -54,3 +54,24 @@ def test_context_stays_usable_after_a_timeout():
     torch.cuda.synchronize()
     assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
     assert torch.equal(l0.view(torch.int32), l1.view(torch.int32))
+
+
+def test_v_outside_fp16_range_is_reported():
+    """The forward's P V runs in fp16: a V value of magnitude 65536 or more cannot be held
+    there, and the converter reports it as FOX_ERR_DEVICE (the other outputs are then not
+    meaningful; nothing faults)."""
+    import forget_gated_softmax_gb300 as fox
+
+    w = wl.Workload("vrange", 1, 300, 2, 64, "bf16", seed=6, gate="normal", lo=1.0)
+    t = to_torch(wl.draw(w), "bf16")
+    p = fox.make_params(w.B, w.N, w.H, w.d)
+    ws = fox.workspace(fox.fox_fwd_workspace_bytes(p), "cuda")
+    fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], ws=ws)
+    assert fox.fox_check_error(ws) == 0
+    v = t["v"].clone()
+    v[0, 137, 1, 5] = 1.0e6
+    fox.fox_fwd(t["q"], t["k"], v, t["z"], ws=ws)
+    assert fox.fox_check_error(ws) == 6  # FOX_ERR_DEVICE
+    v[0, 137, 1, 5] = 65280.0  # the largest bf16 value below 65536 still converts exactly
+    fox.fox_fwd(t["q"], t["k"], v, t["z"], ws=ws)
+    assert fox.fox_check_error(ws) == 0

@@ -2,9 +2,10 @@
 """Benchmark of the forget-gated causal attention hot path on GB300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-gate scan + fused forward (O, LSE), then gate scan + backward rows + fused
-backward + dQ conversion + reverse gate scan (dQ, dK, dV, dz). Throughput is
-nominal causal FLOPs (2 B H N^2 d forward, 5 B H N^2 d backward) per second.
+gate scan + fused forward (O, LSE), then (reading the forward's gate terms from
+the shared workspace) backward rows + fused backward + dQ conversion + reverse
+gate scan (dQ, dK, dV, dz). Throughput is nominal causal FLOPs (2 B H N^2 d
+forward, 5 B H N^2 d backward) per second.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fox|reference]
 
@@ -358,18 +359,18 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dz = torch.empty_like(lse)
     pf = fox.make_params(w.B, w.N, w.H, w.d, 0, 0.0, False)
-    ws_f = fox.workspace(fox.fox_fwd_workspace_bytes(pf), "cuda")
-    ws_b = fox.workspace(fox.fox_bwd_workspace_bytes(pf), "cuda")
+    # One workspace for the step: the backward reads the gate terms the forward left in it.
+    ws_f = ws_b = fox.workspace(max(fox.fox_fwd_workspace_bytes(pf), fox.fox_bwd_workspace_bytes(pf)), "cuda")
     stream = torch.cuda.current_stream()
 
     def step():
         fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_f, stream=stream)
-        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream, gate_ready=True)
 
     for i in range(args.warmup):
         step()
         if i == 0:
-            assert fox.fox_check_error(ws_f) == 0 and fox.fox_check_error(ws_b) == 0, "device-side error"
+            assert fox.fox_check_error(ws_f) == 0, "device-side error"
     torch.cuda.synchronize()
 
     # ---------------- device-resident timed region
@@ -415,8 +416,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
         "dq_zero": ("hbm", w.tokens * 4 * w.d),  # the dQ accumulator cleared (a stream-ordered memset)
         "bwd_rows": ("hbm", w.tokens * (2 * w.d * 2 + 4 + 4 + 4 + 4 + 4)),  # O, dO, lse, rowloc in; delta, rho, R out
         "bwd_dq": ("hbm", w.tokens * w.d * (4 + 2)),
-        "bwd_gate_blocks": ("hbm", w.tokens * (4 + 4)),  # R, C in
-        "bwd_gate": ("hbm", w.tokens * (4 + 4 + 4 + 4)),  # R, C, z in; dz out
+        "bwd_gate": ("hbm", w.tokens * (4 + 4 + 4 + 4)),  # R, C, z in; dz out (one pass)
     }
     kernels = {}
     for name, ms in per.items():  # (dq_zero is a cudaMemsetAsync, listed for its time)
@@ -484,7 +484,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
             di, do_ = dev_in[slot], dev_out[slot]
             fox.fox_fwd(di["q"], di["k"], di["v"], di["z"], o=do_["o"], lse=do_["lse"], ws=ws_f, stream=s_comp)
             fox.fox_bwd(di["q"], di["k"], di["v"], di["z"], do_["o"], do_["lse"], di["dO"], dq=do_["dq"],
-                        dk=do_["dk"], dv=do_["dv"], dz=do_["dz"], ws=ws_b, stream=s_comp)
+                        dk=do_["dk"], dv=do_["dv"], dz=do_["dz"], ws=ws_b, stream=s_comp, gate_ready=True)
             ev_comp[i] = torch.cuda.Event()
             ev_comp[i].record(s_comp)
             with torch.cuda.stream(s_out):
@@ -529,12 +529,12 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     # Decay-aware tile skipping (causal, bit-identical outputs): the same step with
     # tile_skip = 1, on the same inputs; nominal FLOPs over its time is the effective rate.
     ps = fox.make_params(w.B, w.N, w.H, w.d, 0, 0.0, False, tile_skip=True)
-    ws_sf = fox.workspace(fox.fox_fwd_workspace_bytes(ps), "cuda")
-    ws_sb = fox.workspace(fox.fox_bwd_workspace_bytes(ps), "cuda")
+    ws_sf = ws_sb = fox.workspace(max(fox.fox_fwd_workspace_bytes(ps), fox.fox_bwd_workspace_bytes(ps)), "cuda")
 
     def skip_step():
         fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_sf, stream=stream, tile_skip=True)
-        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_sb, stream=stream, tile_skip=True)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_sb, stream=stream, tile_skip=True,
+                    gate_ready=True)
 
     extra["tile_skip"] = timed_variant(fox, torch, stream, skip_step, 10, w.fwd_flops() + w.bwd_flops())
     assert fox.fox_check_error(ws_sf) == 0 and fox.fox_check_error(ws_sb) == 0, "device-side error"
@@ -547,7 +547,8 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     # Non-causal (encoder) mode on the same inputs: every key for every query.
     def nc_step():
         fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_f, stream=stream, non_causal=True)
-        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream, non_causal=True)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream, non_causal=True,
+                    gate_ready=True)
 
     nc_flops = 2 * (w.fwd_flops() + w.bwd_flops())  # the full N^2 score matrix instead of its causal half
     extra["non_causal"] = timed_variant(fox, torch, stream, nc_step, 5, nc_flops)
@@ -598,7 +599,7 @@ def run_fox(args, rank: int, world: int, local_rank: int):
     grad_res = timed_variant(fox, torch, stream, lambda: fox.fox_gate_bwd(zl, Rl, Cl, dz=dzl, ws=ws_gb, stream=stream),
                              10, 0.0)
     grad_ms = sum(grad_res["kernel_ms_per_step"].values())
-    grad_bytes = big * (4 + 4 + 4 + 4)  # R, C, z in; dz out (the block-sum pass re-reads R and C)
+    grad_bytes = big * (4 + 4 + 4 + 4)  # R, C, z in; dz out (one pass)
     extra["gate_steps_large"] = {
         "shape": f"B{GB} H{GH} N{GN} (z ~ N(2,1) fp32, R, C ~ N(0,1))",
         "scan": {"ms": scan_ms, "kernel_ms": scan_res["kernel_ms_per_step"],
@@ -666,13 +667,12 @@ def run_profile(args):
     o, lse = torch.empty_like(q), torch.empty((w.B, w.N, w.H), dtype=torch.float32, device="cuda")
     dq, dk, dv, dz = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(lse)
     pf = fox.make_params(w.B, w.N, w.H, w.d)
-    ws_f = fox.workspace(fox.fox_fwd_workspace_bytes(pf), "cuda")
-    ws_b = fox.workspace(fox.fox_bwd_workspace_bytes(pf), "cuda")
+    ws_f = ws_b = fox.workspace(max(fox.fox_fwd_workspace_bytes(pf), fox.fox_bwd_workspace_bytes(pf)), "cuda")
     stream = torch.cuda.current_stream()
 
     def step():
         fox.fox_fwd(q, k, v, z, o=o, lse=lse, ws=ws_f, stream=stream)
-        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream)
+        fox.fox_bwd(q, k, v, z, o, lse, dO, dq=dq, dk=dk, dv=dv, dz=dz, ws=ws_b, stream=stream, gate_ready=True)
 
     for _ in range(args.warmup):
         step()

@@ -75,6 +75,7 @@ class fox_params(ctypes.Structure):
         ("bias_from_j", ctypes.c_int),
         ("non_causal", ctypes.c_int),
         ("tile_skip", ctypes.c_int),
+        ("gate_ready", ctypes.c_int),
     ]
 
 
@@ -153,9 +154,9 @@ def fox_status_string(status: int) -> str:
 
 
 def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False, non_causal=False,
-                tile_skip=False) -> fox_params:
+                tile_skip=False, gate_ready=False) -> fox_params:
     return fox_params(int(B), int(N), int(H), int(d), int(dtype), float(scale), int(bool(bias_from_j)),
-                      int(bool(non_causal)), int(bool(tile_skip)))
+                      int(bool(non_causal)), int(bool(tile_skip)), int(bool(gate_ready)))
 
 
 def fox_fwd_workspace_bytes(params: fox_params) -> int:
@@ -252,6 +253,7 @@ def fox_bwd(
     bias_from_j: bool = False,
     non_causal: bool = False,
     tile_skip: bool = False,
+    gate_ready: bool = False,
     dq=None,
     dk=None,
     dv=None,
@@ -259,10 +261,13 @@ def fox_bwd(
     ws=None,
     stream=None,
 ):
-    """Backward (bf16): returns (dQ, dK, dV, dz); dz is fp32 [B, N, H]."""
+    """Backward (bf16): returns (dQ, dK, dV, dz); dz is fp32 [B, N, H]. gate_ready: `ws` holds the
+    gate terms of z from a forward on the same workspace (see fox_params.gate_ready)."""
     torch = _torch()
     B, N, H, d = q.shape
-    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal, tile_skip)
+    params = make_params(B, N, H, d, _dtype_code(q), scale, bias_from_j, non_causal, tile_skip, gate_ready)
+    if gate_ready and ws is None:
+        raise ValueError("gate_ready needs the workspace the forward wrote its gate terms into")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

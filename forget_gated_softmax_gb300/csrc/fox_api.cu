@@ -129,6 +129,7 @@ fox_status check_params(const fox_params* p) {
   if (p->bias_from_j != 0 && p->bias_from_j != 1) return FOX_ERR_INVALID_ARG;
   if (p->non_causal != 0 && p->non_causal != 1) return FOX_ERR_INVALID_ARG;
   if (p->tile_skip != 0 && p->tile_skip != 1) return FOX_ERR_INVALID_ARG;
+  if (p->gate_ready != 0 && p->gate_ready != 1) return FOX_ERR_INVALID_ARG;
   if (!(p->scale >= 0.f) || std::isinf(p->scale)) return FOX_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return FOX_ERR_UNSUPPORTED;
   if (p->tile_skip && (p->non_causal || p->dtype != FOX_DTYPE_BF16)) return FOX_ERR_UNSUPPORTED;
@@ -300,7 +301,10 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   st = check_workspace(workspace, workspace_bytes, w.end);
   if (st != FOX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
+  // With gate_ready the workspace holds the forward's gate terms of this z (the caller's contract).
+  if (!p->gate_ready &&
+      launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess)
+    return FOX_ERR_CUDA;
   if (p->tile_skip &&
       launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
     return FOX_ERR_CUDA;
@@ -417,8 +421,7 @@ fox_status fox_gate_scan(const fox_params* p, const float* z, float* c, void* wo
 size_t fox_gate_bwd_workspace_bytes(const fox_params* p) {
   if (check_gate_params(p) != FOX_OK) return 0;
   const size_t nT = ((size_t)p->N + kTile - 1) / kTile;
-  const size_t bytes = sizeof(float) * (size_t)p->B * p->H * nT;
-  return bytes < 256 ? 256 : align_up(bytes, 256);
+  return kErrWordBytes + align_up(kGateStatBytes * (size_t)p->B * p->H * nT, 256);
 }
 
 fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, const float* C, float* dz,
@@ -428,10 +431,16 @@ fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, con
   if (p->B == 0 || p->H == 0 || p->N == 0) return FOX_OK;
   if (!z || !R || !C || !dz || !aligned(z, 4) || !aligned(R, 4) || !aligned(C, 4) || !aligned(dz, 4))
     return FOX_ERR_INVALID_ARG;
-  st = check_workspace(workspace, workspace_bytes, fox_gate_bwd_workspace_bytes(p));
+  const size_t need = fox_gate_bwd_workspace_bytes(p);
+  st = check_workspace(workspace, workspace_bytes, need);
   if (st != FOX_OK) return st;
-  return launch_gate_bwd(p->B, p->N, p->H, p->N, p->bias_from_j, C, R, z, dz, static_cast<float*>(workspace),
-                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  // error word, ticket counter and look-back status records all start at zero
+  if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return FOX_ERR_CUDA;
+  return launch_gate_bwd(p->B, p->N, p->H, p->N, p->bias_from_j, C, R, z, dz, ws + kErrWordBytes,
+                         reinterpret_cast<unsigned*>(ws + kTicketOffset), reinterpret_cast<uint32_t*>(ws), s) ==
+                 cudaSuccess
              ? FOX_OK
              : FOX_ERR_CUDA;
 }

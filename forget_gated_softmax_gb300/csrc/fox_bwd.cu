@@ -22,7 +22,8 @@
 //                 dQ reduced into an fp32 accumulator; the row sums R_i and column sums
 //                 C_j of dS (added into global accumulators)
 //   bwd_dq        dQ = scale * accumulator -> bf16
-//   bwd_gate      reverse prefix scan of (R - C) and the sigmoid chain rule -> dz
+//   bwd_gate      reverse prefix scan of (R - C) (one pass, decoupled look-back) and the sigmoid
+//                 chain rule -> dz
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -45,14 +46,16 @@ namespace {
 // with i < N, taken in the [B, N, H] order of O, dO and LSE so that their loads are contiguous:
 // a warp takes 8 consecutive rows, D / 8 lanes per row, each lane one 16-byte piece of O and
 // of dO per row, all issued before the arithmetic. The padding rows N <= i < Npad of every
-// (b, h) get Delta = 0, rho = +inf and R = 0 from a grid-stride loop over the same threads.
-// (The dQ accumulator is zeroed by a memset before this kernel.)
+// (b, h) get Delta = 0, rho = +inf and R = 0 from a grid-stride loop over the same threads, which
+// also clears the gate gradient's status records and ticket counter. (The dQ accumulator is
+// zeroed by a memset before this kernel.)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int Npad, const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                                                       const float* __restrict__ rowloc, float* __restrict__ delta,
                                                       float* __restrict__ rho, float* __restrict__ rowsum,
-                                                      int delta_ready) {
+                                                      int delta_ready, uint4* __restrict__ gstat, size_t gstat16,
+                                                      unsigned* __restrict__ ticket) {
   constexpr int LPR = D / 8;          // lanes per row
   constexpr int RPI = 32 / LPR;       // rows per load instruction
   constexpr int LOADS = 8 / RPI;      // loads per lane per tensor
@@ -109,6 +112,10 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
       rho[r] = lse[row] * kLog2e - rowloc[r];
     }
   }
+  // the gate gradient's look-back status records and ticket counter start at zero
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < gstat16; q += (size_t)gridDim.x * blockDim.x)
+    gstat[q] = make_uint4(0u, 0u, 0u, 0u);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
   const long long pads = (long long)B * H * (Npad - N);
   for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < pads; q += (long long)gridDim.x * blockDim.x) {
     const long long bh = q / (Npad - N);
@@ -780,15 +787,25 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Np
 }
 
 // ---------------------------------------------------------- gate backward
-// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz_t = d a_t sigmoid(-z_t), in two
-// launches so that the loads of R, C, z and dz are coalesced and every SM takes part:
-//   1. gate_grad_block_kernel: warp per (b h, 128-token block): the block's sum of R - C;
-//   2. gate_grad_final_kernel: CTA per (128-token block, b, 32 heads): the carry from the
-//      later blocks (summed in fp64), the suffix scan inside the block, then dz over
-//      (token, head) so that the [B, N, H] accesses run along the heads.
-// R and C rows hold `stride` floats per (b, h); tokens past N count as 0.
+// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz_t = d a_t sigmoid(-z_t): a suffix
+// scan along the sequence per (b, h), in one pass over R, C, z and dz (16 bytes per token and
+// head) with a decoupled look-back across 128-token blocks:
+//   - CTAs take tickets from a counter in the order blocks k = nT-1, nT-2, ..., 0 (the batches
+//     and head groups of one k together), so every block a CTA waits on has already started;
+//   - a CTA (block k, batch b, 32 heads) loads its R and C rows (coalesced along the tokens),
+//     forms each head's block total of R - C and publishes it as the block's aggregate;
+//   - it then sums the aggregates of the later blocks k+1, k+2, ... until it meets one whose
+//     inclusive suffix sum is already published (32 blocks per round, one per lane), adds its
+//     own total and publishes its inclusive suffix sum, in double-float (fp32 hi/lo pairs
+//     with TwoSum: about 48 bits; fp64 runs at a small fraction of the fp32 rate here);
+//   - the carry and the block-local suffix scan give d a, and dz is written along the heads
+//     (coalesced [B, N, H] accesses).
+// Each published value shares one 64-bit word with its ready flag (flag in the high half), so
+// a reader that sees the flag sees the value. The status words and the ticket counter must be
+// zero before the launch. A wait that runs out (one second) sets DEV_ERR_TIMEOUT_SYNC and the
+// block goes on with what it has, so nothing waits forever.
 // (hi, lo) += (bhi, blo) in double-float: Knuth's TwoSum on the high parts, the low parts
-// added in fp32, renormalised with Dekker's FastTwoSum (about 48 significant bits).
+// added in fp32, renormalised with Dekker's FastTwoSum.
 __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float bhi, float blo) {
   const float s = hi + bhi;
   const float bb = s - hi;
@@ -797,67 +814,55 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float bhi, flo
   lo = e - (hi - s);
 }
 
-__global__ void __launch_bounds__(256) gate_grad_block_kernel(int BH, int N, int nT, int stride,
-                                                             const float* __restrict__ colsum,
-                                                             const float* __restrict__ rowsum,
-                                                             float* __restrict__ blocktot) {
-  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= (long long)BH * nT) return;
-  const size_t bh = (size_t)(wid / nT);
-  const int k = (int)(wid % nT);
-  const float* R = rowsum + bh * stride;
-  const float* C = colsum + bh * stride;
-  float x = 0.f;
-#pragma unroll
-  for (int e = 0; e < kTile / 32; ++e) {
-    const int t = k * kTile + e * 32 + lane;
-    if (t < N) x += R[t] - C[t];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  if (lane == 0) blocktot[bh * nT + k] = x;
+// Status record of one (b h, block): the block total (aggregate) and the inclusive suffix sum
+// (hi, lo), each 64-bit word = (1 << 32) | float bits once published.
+struct GateStat {
+  unsigned long long agg, inc_hi, inc_lo, pad;
+};
+__device__ __forceinline__ unsigned long long stat_word(float v) {
+  return (1ull << 32) | static_cast<unsigned long long>(__float_as_uint(v));
+}
+__device__ __forceinline__ void stat_store(unsigned long long* w, float v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(w), "l"(stat_word(v)) : "memory");
+}
+__device__ __forceinline__ unsigned long long stat_load(const unsigned long long* w) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(w) : "memory");
+  return v;
 }
 
-__global__ void __launch_bounds__(256) gate_grad_final_kernel(int N, int H, int nT, int stride, int bias_from_j,
-                                                             const float* __restrict__ colsum,
-                                                             const float* __restrict__ rowsum,
-                                                             const float* __restrict__ blocktot,
-                                                             const float* __restrict__ z, float* __restrict__ dz) {
-  constexpr int kPer = kTile * 32 / 256;  // elements per thread of the (token, head) tile
-  __shared__ float xs[32][kTile + 1];     // [head][token]: R - C, then d a
-  __shared__ float cs[32][kTile + 1];     // C (bias_from_j)
-  __shared__ float carry[32];
-  const int k = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * 32;
-  const int nh = min(32, H - h0);
+constexpr int kGateHeads = 32;     // heads per gate-gradient CTA
+constexpr int kGateThreads = 512;  // 16 warps, two heads each
+constexpr int kLookLanes = 16;     // lanes (blocks read per round) of one head's look-back
+
+__global__ void __launch_bounds__(kGateThreads) gate_grad_kernel(int B, int N, int H, int nT, int stride,
+                                                                 int bias_from_j, const float* __restrict__ colsum,
+                                                                 const float* __restrict__ rowsum,
+                                                                 const float* __restrict__ z, float* __restrict__ dz,
+                                                                 GateStat* __restrict__ stat, unsigned* ticket,
+                                                                 uint32_t* err) {
+  constexpr int kPer = kTile * kGateHeads / kGateThreads;  // elements per thread of the (token, head) tile
+  __shared__ float xs[kGateHeads][kTile + 1];               // [head][token]: R - C, then d a
+  __shared__ float cs[kGateHeads][kTile + 1];               // C (bias_from_j)
+  __shared__ unsigned s_ticket;
+  if (threadIdx.x == 0) s_ticket = atomicAdd(ticket, 1u);
+  __syncthreads();
+  const int HG = (H + kGateHeads - 1) / kGateHeads;
+  const int per_k = B * HG;
+  const int k = nT - 1 - static_cast<int>(s_ticket) / per_k;
+  const int r = static_cast<int>(s_ticket) % per_k;
+  const int b = r / HG, h0 = (r % HG) * kGateHeads;
+  const int nh = min(kGateHeads, H - h0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = k * kTile;
+  // All loads first: R and C rows (thread e covers token e % 128 of head e / 128, rows contiguous
+  // per head) and z along the heads (token e / 32, head e % 32), for the dz pass at the end.
+  float zv[kPer];
   {
-    // carry of head hh: the later blocks' totals, summed by 8 threads in double-float (hi + lo
-    // fp32 pairs added with TwoSum), four loads issued before their additions
-    const int hh = threadIdx.x >> 3, part = threadIdx.x & 7;
-    float chi = 0.f, clo = 0.f;
-    if (hh < nh) {
-      const float* tot = blocktot + ((size_t)b * H + h0 + hh) * nT;
-      for (int kk0 = k + 1 + part; kk0 < nT; kk0 += 32) {
-        float v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = kk0 + 8 * q < nT ? tot[kk0 + 8 * q] : 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) two_sum_acc(chi, clo, v[q], 0.f);
-      }
-    }
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1)
-      two_sum_acc(chi, clo, __shfl_xor_sync(0xffffffffu, chi, o), __shfl_xor_sync(0xffffffffu, clo, o));
-    if (part == 0 && hh < nh) carry[hh] = chi + clo;
-  }
-  {
-    // R, C: thread e covers token e % 128 of head e / 128 (rows contiguous per head); loads first
     float rv[kPer], cv[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int e = threadIdx.x + u * 256, hh = e / kTile, t = e % kTile;
+      const int e = threadIdx.x + u * kGateThreads, hh = e / kTile, t = e % kTile;
       const bool in = hh < nh && t0 + t < N;
       const size_t off = ((size_t)b * H + h0 + hh) * stride + t0 + t;
       rv[u] = in ? rowsum[off] : 0.f;
@@ -865,19 +870,27 @@ __global__ void __launch_bounds__(256) gate_grad_final_kernel(int N, int H, int 
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int e = threadIdx.x + u * 256, hh = e / kTile, t = e % kTile;
+      const int e = threadIdx.x + u * kGateThreads, t = e >> 5, hh = e & 31;
+      zv[u] = (hh < nh && t0 + t < N) ? z[((size_t)b * N + t0 + t) * H + h0 + hh] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * kGateThreads, hh = e / kTile, t = e % kTile;
       xs[hh][t] = rv[u] - cv[u];
       cs[hh][t] = cv[u];
     }
   }
   __syncthreads();
-  for (int hh = warp; hh < nh; hh += 8) {
-    // lane holds tokens 4 lane .. 4 lane + 3: suffix inside the lane, then over the later lanes
-    float v[4], run = 0.f;
+  // Heads 2 warp and 2 warp + 1: lane holds tokens 4 lane .. 4 lane + 3 of each.
+  float v[2][4], lane_later[2], lane_run[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int hh = 2 * warp + q;
+    float run = 0.f;
 #pragma unroll
     for (int e = 3; e >= 0; --e) {
-      run += xs[hh][4 * lane + e];
-      v[e] = run;
+      run += hh < nh ? xs[hh][4 * lane + e] : 0.f;
+      v[q][e] = run;
     }
     float later = run;  // inclusive suffix over lanes lane .. 31 of the lane totals
 #pragma unroll
@@ -885,28 +898,95 @@ __global__ void __launch_bounds__(256) gate_grad_final_kernel(int N, int H, int 
       const float y = __shfl_down_sync(0xffffffffu, later, o);
       if (lane + o < 32) later += y;
     }
-    const float base = later - run + carry[hh];  // lanes after this one, then the later blocks
+    lane_later[q] = later;
+    lane_run[q] = run;
+    // lane 0's suffix is the block total: publish it (the last block's is also its inclusive sum)
+    if (lane == 0 && hh < nh) {
+      GateStat* st = stat + ((size_t)b * H + h0 + hh) * nT + k;
+      stat_store(&st->agg, later);
+      if (k == nT - 1) {
+        stat_store(&st->inc_lo, 0.f);
+        stat_store(&st->inc_hi, later);
+      }
+    }
+  }
+  // Look-back of both heads at once: lanes 16 g .. 16 g + 15 read blocks j0 + (lane % 16) of head
+  // 2 warp + g, summing aggregates up to the first block whose inclusive sum is published.
+  const int g = lane >> 4, gl = lane & 15;
+  const int hh_g = 2 * warp + g;
+  const GateStat* row = stat + ((size_t)b * H + h0 + min(hh_g, nh - 1)) * nT;
+  float chi = 0.f, clo = 0.f;  // the carry of head hh_g (valid in every lane of the group)
+  bool done = hh_g >= nh || k == nT - 1;
+  int j0 = k + 1;
+  bool timed_out = false;
+  const uint64_t t_start = globaltimer_ns();
+  for (uint32_t it = 0; __any_sync(0xffffffffu, !done); ++it) {
+    const int j = j0 + gl;
+    unsigned long long ih = 0, il = 0, ag = 0;
+    if (!done && j < nT) {
+      ih = stat_load(&row[j].inc_hi);
+      il = stat_load(&row[j].inc_lo);
+      ag = stat_load(&row[j].agg);
+    }
+    const bool have_inc = (ih >> 32) != 0 && (il >> 32) != 0;
+    const bool have_agg = (ag >> 32) != 0;
+    const unsigned inc_all = __ballot_sync(0xffffffffu, !done && j < nT && have_inc);
+    const unsigned rdy_all = __ballot_sync(0xffffffffu, j >= nT || have_inc || have_agg);
+    const unsigned inc = (inc_all >> (16 * g)) & 0xFFFFu, rdy = (rdy_all >> (16 * g)) & 0xFFFFu;
+    // lanes up to the group's first inclusive one (or all 16) must be ready
+    const unsigned need = inc ? ((inc & (0u - inc)) * 2u - 1u) : 0xFFFFu;
+    const bool resolved = !done && (rdy & need) == need;
+    float hi = 0.f, lo = 0.f;
+    if (resolved && j < nT && ((need >> gl) & 1u)) {
+      const bool first_inc = inc != 0 && gl == __ffs(inc) - 1;
+      hi = __uint_as_float(static_cast<uint32_t>(first_inc ? ih : ag));
+      lo = first_inc ? __uint_as_float(static_cast<uint32_t>(il)) : 0.f;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)  // within the 16-lane group
+      two_sum_acc(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    if (resolved) {
+      two_sum_acc(chi, clo, hi, lo);
+      j0 += kLookLanes;
+      done = inc != 0 || j0 >= nT;
+    }
+    if ((it & 31u) == 31u && __any_sync(0xffffffffu, globaltimer_ns() - t_start > FOX_WAIT_TIMEOUT_NS)) {
+      timed_out = timed_out || !done;
+      break;
+    }
+  }
+  if (timed_out && gl == 0 && err) atomicOr(err, DEV_ERR_TIMEOUT_SYNC);
+  const float carry_g = chi + clo;
+  // the block totals of both heads (lane 0's suffixes), for the group of each
+  const float tot0 = __shfl_sync(0xffffffffu, lane_later[0], 0), tot1 = __shfl_sync(0xffffffffu, lane_later[1], 0);
+  if (gl == 0 && hh_g < nh && k < nT - 1) {
+    // inclusive = carry + this block's total
+    float ihi = chi, ilo = clo;
+    two_sum_acc(ihi, ilo, g ? tot1 : tot0, 0.f);
+    GateStat* st = stat + ((size_t)b * H + h0 + hh_g) * nT + k;
+    stat_store(&st->inc_lo, ilo);
+    stat_store(&st->inc_hi, ihi);
+  }
+  // d a inside the block: this lane's suffix, the later lanes, then the later blocks
+  const float carry_h[2] = {__shfl_sync(0xffffffffu, carry_g, 0), __shfl_sync(0xffffffffu, carry_g, 16)};
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int hh = 2 * warp + q;
+    if (hh >= nh) break;
+    const float base = lane_later[q] - lane_run[q] + carry_h[q];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int t = 4 * lane + e;
-      xs[hh][t] = bias_from_j ? v[e] + base + cs[hh][t] : v[e] + base;
+      xs[hh][t] = bias_from_j ? v[q][e] + base + cs[hh][t] : v[q][e] + base;
     }
   }
   __syncthreads();
-  {
-    // dz over (token, head), heads fastest: the [B, N, H] loads and stores run along the heads
-    float zv[kPer];
+  // dz over (token, head), heads fastest: the [B, N, H] stores run along the heads
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = threadIdx.x + u * 256, t = e >> 5, hh = e & 31;
-      zv[u] = (hh < nh && t0 + t < N) ? z[((size_t)b * N + t0 + t) * H + h0 + hh] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = threadIdx.x + u * 256, t = e >> 5, hh = e & 31;
-      if (hh < nh && t0 + t < N)
-        dz[((size_t)b * N + t0 + t) * H + h0 + hh] = xs[hh][t] / (1.f + expf(zv[u]));  // d a sigmoid(-z)
-    }
+  for (int u = 0; u < kPer; ++u) {
+    const int e = threadIdx.x + u * kGateThreads, t = e >> 5, hh = e & 31;
+    if (hh < nh && t0 + t < N)
+      dz[((size_t)b * N + t0 + t) * H + h0 + hh] = xs[hh][t] / (1.f + expf(zv[u]));  // d a sigmoid(-z)
   }
 }
 
@@ -933,7 +1013,8 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
     const long long octets = ((long long)a.B * a.N * a.H + 7) / 8;  // 8 rows per warp, 8 warps per block
     bwd_rows_kernel<D><<<(unsigned)((octets + 7) / 8), 256, 0, s>>>(
         a.B, a.N, a.H, g.Npad, static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        rowloc, delta, rho, rowsum, a.delta_ready);
+        rowloc, delta, rho, rowsum, a.delta_ready, reinterpret_cast<uint4*>(a.ws + w.gstat),
+        kGateStatBytes * (size_t)g.BH * g.nT / 16, reinterpret_cast<unsigned*>(a.ws + kTicketOffset));
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -975,29 +1056,24 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // the gate scan's tile totals are consumed by now: their buffer holds the block sums of R - C
-  return launch_gate_bwd(a.B, a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz,
-                         reinterpret_cast<float*>(a.ws + g.tiletot), s);
+  return launch_gate_bwd(a.B, a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz, a.ws + w.gstat,
+                         reinterpret_cast<unsigned*>(a.ws + kTicketOffset), err, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
-                            const float* rowsum, const float* z, float* dz, float* blocktot, cudaStream_t s) {
+                            const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
+                            uint32_t* err, cudaStream_t s) {
   const long long BH = (long long)B * H;
   if (BH == 0 || N == 0) return cudaSuccess;
   const int nT = (N + kTile - 1) / kTile;
-  {
-    TraceScope trace("bwd_gate_blocks", s);
-    gate_grad_block_kernel<<<(unsigned)((BH * nT + 7) / 8), 256, 0, s>>>((int)BH, N, nT, stride, colsum, rowsum,
-                                                                          blocktot);
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const long long ctas = (long long)nT * B * ((H + kGateHeads - 1) / kGateHeads);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("bwd_gate", s);
-    gate_grad_final_kernel<<<dim3((unsigned)nT, (unsigned)B, (unsigned)((H + 31) / 32)), 256, 0, s>>>(
-        N, H, nT, stride, bias_from_j, colsum, rowsum, blocktot, z, dz);
+    gate_grad_kernel<<<(unsigned)ctas, kGateThreads, 0, s>>>(B, N, H, nT, stride, bias_from_j, colsum, rowsum, z, dz,
+                                                    static_cast<GateStat*>(stat), ticket, err);
   }
   return cudaGetLastError();
 }

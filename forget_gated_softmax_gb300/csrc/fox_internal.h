@@ -40,10 +40,13 @@ struct BwdLayout {
   size_t colsum = 0;  // float [BH][Npad]   C_j = sum_i dS_ij
   size_t rowsum = 0;  // float [BH][Npad]   R_i = sum_j dS_ij (0 in exact arithmetic; accumulated across key tiles)
   size_t dqacc = 0;   // float [BH][Npad][d] dQ accumulator (fp32, unscaled)
+  size_t gstat = 0;   // [BH][nT] 32-byte status records of the gate gradient's look-back
   size_t end = 0;
 };
 
 constexpr size_t kErrWordBytes = 256;  // workspace header: uint32 error word + padding
+constexpr size_t kTicketOffset = 128;  // header byte offset of the gate gradient's ticket counter
+constexpr size_t kGateStatBytes = 32;  // bytes per (b h, 128-token block) look-back status record
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -89,6 +92,8 @@ inline BwdLayout bwd_layout(const GateLayout& g, int d) {
   off = align_up(off + row, 256);
   w.dqacc = off;
   off = align_up(off + row * (size_t)d, 256);
+  w.gstat = off;
+  off = align_up(off + kGateStatBytes * (size_t)g.BH * g.nT, 256);
   w.end = off;
   return w;
 }
@@ -107,10 +112,12 @@ struct TraceScope {
 // ---- launchers (return cudaGetLastError() of the launch) ----
 // c[b,t,h] = (base_T + local_t) / log2 e from the gate terms in the workspace (fp64 sum, fp32 out).
 cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, int N, int H, float* c, cudaStream_t s);
-// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz = d a_t sigmoid(-z); R and C rows of
-// `stride` floats per (b, h); blocktot is scratch of B * H * ceil(N / 128) floats.
+// d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz = d a_t sigmoid(-z), in one pass with a
+// decoupled look-back; R and C rows of `stride` floats per (b, h). `stat` (B * H * ceil(N / 128)
+// records of kGateStatBytes) and `ticket` must be zero at the launch; err is the error word.
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
-                            const float* rowsum, const float* z, float* dz, float* blocktot, cudaStream_t s);
+                            const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
+                            uint32_t* err, cudaStream_t s);
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
                              cudaStream_t s);
 

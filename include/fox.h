@@ -79,6 +79,15 @@ typedef struct fox_params {
                       largest (see fox_tile_span); outputs are bit-identical to tile_skip = 0 for
                       the forward, dK and dV, and equal up to the order of fp32 atomic sums for dQ
                       and dz. Causal bf16 only (FOX_ERR_UNSUPPORTED otherwise). */
+  int gate_ready;  /* fox_bwd only (ignored elsewhere). 0: the backward runs its own gate scan (default).
+                      1: the workspace already holds the gate terms of this z, written by a fox_fwd
+                      (or fox_fwd_xgate, fox_gate_proj, fox_gate_scan) call with the same B, N, H and
+                      bias_from_j on the same workspace, and nothing has written the workspace since:
+                      the backward skips the scan and reads them. The workspace must then be at least
+                      the larger of the fox_fwd and fox_bwd sizes. The backward also leaves the
+                      workspace's error word as the forward left it (errors of both calls accumulate
+                      until fox_check_error clears them). With a workspace that does not hold them, the
+                      results are wrong (nothing faults: every index comes from B, N, H). */
 } fox_params;
 
 /* Workspace bytes fox_fwd / fox_bwd need for these params (0 if params are invalid). */
@@ -130,10 +139,11 @@ fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const v
 /*
  * Backward (bf16 only). Reads q, k, v, z, the forward's O and LSE, and the
  * upstream gradient dO; writes dq, dk, dv [B,N,H,d] bf16 and dz [B,N,H] fp32.
- * Steps: gate scan, the fp32 dQ accumulator in the workspace cleared (a
- * stream-ordered cudaMemsetAsync), Delta_i = dO_i . O_i, the fused
- * recompute-and-backward attention kernel (dK, dV, dQ accumulator and the
- * column sums of dS), the dQ conversion and the reverse gate scan.
+ * Steps: gate scan (skipped with p->gate_ready), the fp32 dQ accumulator in the
+ * workspace cleared (a stream-ordered cudaMemsetAsync), Delta_i = dO_i . O_i,
+ * the fused recompute-and-backward attention kernel (dK, dV, dQ accumulator and
+ * the row and column sums of dS), the dQ conversion and the reverse gate scan
+ * (one pass, decoupled look-back across 128-token blocks).
  * With non_causal = 1, Delta is not taken from the bf16 O: a pass of its own
  * forms Delta_i = sum_j P_ij dP_ij from S = Q K^T and dP = dO V^T with P
  * recomputed from LSE, in fp32 (the gate gradient is a small difference of

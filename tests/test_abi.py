@@ -81,6 +81,7 @@ def test_fwd_rejects_bad_arguments_on_host(L):
     assert _fwd(L, fox.fox_params(1, 256, 2, 64, 0, -1.0, 0)) == 1
     assert _fwd(L, fox.fox_params(1, 256, 2, 64, 0, float("nan"), 0)) == 1
     assert _fwd(L, fox.fox_params(1, 256, 2, 64, 0, 0.0, 2)) == 1
+    assert _fwd(L, fox.fox_params(1, 256, 2, 64, 0, 0.0, 0, 0, 0, 2)) == 1  # gate_ready must be 0 or 1
     assert _fwd(L, _p(), q=None) == 1
     assert _fwd(L, _p(), lse=None) == 1
     assert _fwd(L, _p(), q=FAKE + 8) == 1  # TMA needs 16-byte aligned operands

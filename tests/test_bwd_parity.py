@@ -150,6 +150,32 @@ def test_train_workload_backward_16_heads():
     check_heads_blocked(wl.TRAIN_BF16, heads, block=512)
 
 
+@pytest.mark.parametrize("tile_skip", [False, True])
+def test_gate_ready_reuses_the_forward_gate_terms(tile_skip):
+    """fox_bwd with gate_ready on the workspace the forward wrote: no gate scan, the same results
+    (dK, dV bit for bit; dQ and dz up to the order of their fp32 reductions)."""
+    import forget_gated_softmax_gb300 as fox
+
+    w = wl.Workload("bready", 2, 900, 3, 128, "bf16", seed=23, gate="head_uniform", lo=0.0, hi=5.0, backward=True)
+    arrays = wl.draw(w)
+    t = to_torch(arrays, "bf16")
+    p = fox.make_params(w.B, w.N, w.H, w.d, tile_skip=tile_skip)
+    ws = fox.workspace(max(fox.fox_fwd_workspace_bytes(p), fox.fox_bwd_workspace_bytes(p)), "cuda")
+    o, lse = fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], ws=ws, tile_skip=tile_skip)
+    g1 = fox.fox_bwd(t["q"], t["k"], t["v"], t["z"], o, lse, t["dO"], ws=ws, gate_ready=True, tile_skip=tile_skip)
+    assert fox.fox_check_error(ws) == 0
+    g0 = fox.fox_bwd(t["q"], t["k"], t["v"], t["z"], o, lse, t["dO"], tile_skip=tile_skip)
+    torch.cuda.synchronize()
+    g0, g1 = [tensor_f64(x) for x in g0], [tensor_f64(x) for x in g1]
+    np.testing.assert_array_equal(g1[1], g0[1])
+    np.testing.assert_array_equal(g1[2], g0[2])
+    assert rel(g1[0], g0[0]) < 1e-5 and rel(g1[3], g0[3]) < 1e-5
+    x = exact(arrays, "bf16")
+    r = ora.backward_head(x["q"][1, :, 2], x["k"][1, :, 2], x["v"][1, :, 2], x["z"][1, :, 2], x["dO"][1, :, 2])
+    for n in range(4):
+        assert rel(g1[n][1, :, 2], r[n]) <= TOL_GRAD_REL
+
+
 def test_backward_determinism():
     """dK and dV are written without atomics and repeat bit for bit; dQ and dz
     take fp32 atomic reductions across key tiles and repeat within rounding."""

@@ -54,12 +54,14 @@ def test_gate_scan_workspace_only():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("N", [1, 5, 1023, 1024, 1025, 3000])
+@pytest.mark.parametrize("B,N,H", [(2, 1, 3), (2, 5, 3), (2, 1023, 3), (2, 1024, 3), (2, 1025, 3), (2, 3000, 3),
+                                   (3, 8193, 40), (1, 16384, 32)])
 @pytest.mark.parametrize("from_j", [False, True])
-def test_gate_bwd_from_sums(N, from_j):
+def test_gate_bwd_from_sums(B, N, H, from_j):
+    """One pass with a look-back across 128-token blocks: up to 128 blocks (four rounds of
+    32), head groups of 32 with a partial one (H = 40), several batches."""
     import forget_gated_softmax_gb300 as fox
 
-    B, H = 2, 3
     r = np.random.default_rng(1000 + N + from_j)
     z = _gates(B, N, H, seed=N + 17)
     R = r.standard_normal((B, H, N)).astype(np.float32)

@@ -308,11 +308,13 @@ fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void
   if (p->tile_skip &&
       launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
     return FOX_ERR_CUDA;
-  CUtensorMap maps[4];
+  CUtensorMap maps[6];
   if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d, 64) ||
       !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d, kTile) ||
       !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d, kTile) ||
-      !make_bnhd_map(&maps[3], dO, p->B, p->N, p->H, p->d, 64))
+      !make_bnhd_map(&maps[3], dO, p->B, p->N, p->H, p->d, 64) ||
+      !make_bnhd_map(&maps[4], dk, p->B, p->N, p->H, p->d, kTile) ||
+      !make_bnhd_map(&maps[5], dv, p->B, p->N, p->H, p->d, kTile))
     return FOX_ERR_CUDA;
   AttnBwdArgs a;
   a.B = p->B;

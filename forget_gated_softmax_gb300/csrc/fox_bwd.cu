@@ -219,25 +219,8 @@ enum BwdBar {
                   // over it read out by the bulk engine (count 4)
 };
 
-// Barrier over `n` threads that also ORs a predicate across them: every thread gets the
-// same answer, so a group can agree to stop without anyone left waiting.
-__device__ __forceinline__ bool named_bar_any(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %3, 0;\n\t"
-      "barrier.red.or.pred po, %1, %2, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"(n), "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ void sts_f32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
@@ -328,6 +311,7 @@ template <int D, bool kExactSums>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fox_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                        const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
                         const BwdKParams p) {
   using L = BwdLayoutSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -707,7 +691,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       named_bar_any(5, 256, false);
       if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
     }
-    // dK, dV epilogue
+    // dK, dV epilogue: scaled, rounded to bf16 and staged in the shared memory of the K and V
+    // tiles (free once every MMA has retired) in the 128-byte-swizzled layout of the output
+    // tensor maps, then written by tensor stores, whole 128-byte row pieces per 64-channel box
+    // (a thread's own 16-byte stores to rows H d apart had cost about 2 us per CTA). The
+    // stores clip rows past N.
     if (ok) ok = mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
@@ -720,7 +708,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int which = 0; which < 2; ++which) {
         const uint32_t src = (which == 0 ? tdK : tdV) + e0;
         const float mul = which == 0 ? p.scale : 1.f;
-        __nv_bfloat16* outp = which == 0 ? p.dk : p.dv;
+        // row jr of the 64-channel box that holds channel e0 (16 KB per box, 128 B per row)
+        const uint32_t row = smem_u32(sm + (which == 0 ? L::kK : L::kV) + (e0 / 64) * 16384) + (uint32_t)jr * 128u;
 #pragma unroll
         for (int c = 0; c < kCols; c += 64) {
           uint32_t r[2][32];
@@ -729,20 +718,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            if (c + 32 * hh >= kCols || j >= p.N) continue;
-            uint4* dst = reinterpret_cast<uint4*>(outp + (((size_t)b * p.N + j) * p.H + h) * D + e0 + c + 32 * hh);
+            if (c + 32 * hh >= kCols) continue;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 0]) * mul, __uint_as_float(r[hh][8 * q4 + 1]) * mul);
-              w.y = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 2]) * mul, __uint_as_float(r[hh][8 * q4 + 3]) * mul);
-              w.z = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 4]) * mul, __uint_as_float(r[hh][8 * q4 + 5]) * mul);
-              w.w = pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 6]) * mul, __uint_as_float(r[hh][8 * q4 + 7]) * mul);
-              dst[q4] = w;
+              const int piece = ((e0 % 64) + c + 32 * hh) / 8 + q4;  // 16-byte piece of the 128-byte row
+              sts_v4(row + (uint32_t)((piece ^ (jr & 7)) << 4),
+                     pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 0]) * mul, __uint_as_float(r[hh][8 * q4 + 1]) * mul),
+                     pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 2]) * mul, __uint_as_float(r[hh][8 * q4 + 3]) * mul),
+                     pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 4]) * mul, __uint_as_float(r[hh][8 * q4 + 5]) * mul),
+                     pack_bf16x2(__uint_as_float(r[hh][8 * q4 + 6]) * mul, __uint_as_float(r[hh][8 * q4 + 7]) * mul));
             }
           }
         }
       }
+      fence_proxy_async_smem();
+    }
+    // The 256 elementwise threads meet (and agree whether every one of them staged its row);
+    // one thread then issues the stores and waits until the bulk engine has read shared memory.
+    if (!named_bar_any(4, 256, !ok) && threadIdx.x == 0) {
+#pragma unroll
+      for (int box = 0; box < D / 64; ++box) {
+        tma_store_4d(&tmap_dk, sm + L::kK + box * 16384, box * 64, h, J * kTile, b);
+        tma_store_4d(&tmap_dv, sm + L::kV + box * 16384, box * 64, h, J * kTile, b);
+      }
+      bulk_commit_group();
+      bulk_wait_read<0>();
     }
   }
 
@@ -1044,7 +1044,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("attn_bwd", s);
-    kernel<<<(unsigned)blocks, kBwdThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], maps[3], p);
+    kernel<<<(unsigned)blocks, kBwdThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

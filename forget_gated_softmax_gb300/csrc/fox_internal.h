@@ -180,7 +180,8 @@ cudaError_t launch_delta_pass(const DeltaArgs& a, const CUtensorMap* maps /* q, 
 // Delta/rho rows, dQ accumulator zeroing, the fused backward kernel, the dQ
 // conversion and the reverse gate scan; the gate scan must already be in ws.
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w,
-                            const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box) */,
+                            const CUtensorMap* maps /* q (64-row box), k, v (128-row box), dO (64-row box),
+                                                       dk, dv (128-row box, stored) */,
                             cudaStream_t s);
 
 // Gate projection z = x W_f^T + b_f (tensor cores) fused with the tile scan, then the base

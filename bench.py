@@ -691,6 +691,32 @@ def run_profile(args):
                     "attn_bwd_tflops": w.bwd_flops() / (per.get("attn_bwd", 0) * 1e-3) / 1e12 if per.get("attn_bwd") else None}))
 
 
+def run_profile_gate(args):
+    """--profile-gate: the two gate steps alone on the large synthetic (B64 H32 N16384: z, R, C and dz
+    are 134 MB each, about 0.6 GB on the device): warmup + steps calls of the gate scan and of the
+    gate gradient, for profiler captures. Not a bench line."""
+    import torch
+
+    import forget_gated_softmax_gb300 as fox
+
+    GB, GN, GH = 64, 16384, 32
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    zl = 2.0 + torch.randn((GB, GN, GH), generator=gen, device="cuda", dtype=torch.float32)
+    Rl = torch.randn((GB, GH, GN), generator=gen, device="cuda", dtype=torch.float32)
+    Cl = torch.randn((GB, GH, GN), generator=gen, device="cuda", dtype=torch.float32)
+    dzl = torch.empty_like(zl)
+    pg = fox.make_params(GB, GN, GH, 64)
+    ws_g = fox.workspace(fox.fox_gate_scan_workspace_bytes(pg), "cuda")
+    ws_gb = fox.workspace(fox.fox_gate_bwd_workspace_bytes(pg), "cuda")
+    for _ in range(args.warmup + args.steps):
+        fox.fox_gate_scan(zl, want_c=False, ws=ws_g)
+        fox.fox_gate_bwd(zl, Rl, Cl, dz=dzl, ws=ws_gb)
+    torch.cuda.synchronize()
+    assert fox.fox_check_error(ws_g) == 0 and fox.fox_check_error(ws_gb) == 0, "device-side error"
+    log(json.dumps({"profile_gate": f"B{GB} H{GH} N{GN}", "calls": args.warmup + args.steps}))
+
+
 def run_configs(args):
     """--configs: forward (and backward where the workload has one) of each named input
     recipe on this GPU, CUDA-event timed; one JSON object per workload on stderr, and the
@@ -770,6 +796,8 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="run only the forward+backward step (warmup + steps calls), for profiler captures; "
                          "prints timings on stderr, not a bench line")
+    ap.add_argument("--profile-gate", action="store_true",
+                    help="run only the gate scan and gate gradient on the large synthetic (profiler captures)")
     ap.add_argument("--shape", default=None,
                     help="B,N,H,d of a smaller case of the same workload recipe (profiling runs; not a bench line)")
     args = ap.parse_args()
@@ -790,6 +818,9 @@ def main():
         return
     if args.profile:
         run_profile(args)
+        return
+    if args.profile_gate:
+        run_profile_gate(args)
         return
     if args.configs:
         run_configs(args)

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(int B, int N, int H, int 
                                                       float* __restrict__ rho, float* __restrict__ rowsum,
                                                       int delta_ready, uint4* __restrict__ gstat, size_t gstat16,
                                                       unsigned* __restrict__ ticket) {
+  grid_dep_trigger();  // the attention kernel may start its prologue and its K, V loads
   constexpr int LPR = D / 8;          // lanes per row
   constexpr int RPI = 32 / LPR;       // rows per load instruction
   constexpr int LOADS = 8 / RPI;      // loads per lane per tensor
@@ -394,19 +395,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
   }
 
+  // This kernel may start while the row kernel before it still runs (launch_dependent): the K and
+  // V tiles are the caller's input and load at once; everything the earlier kernels wrote (the
+  // column record, Delta, rho, the cleared row sums) is read only after grid_dep_wait().
+  if (warp == 12 && lane == 0) {
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    tma_prefetch_desc(&tmap_do);
+    mbar_arrive_expect_tx(&bars[BB_KV], 2 * L::kTileBytes + kColRec * 4);
+    for (int x = 0; x < D / 64; ++x) {
+      tma_load_4d(sm + L::kK + x * 16384, &tmap_k, &bars[BB_KV], x * 64, h, J * kTile, b);
+      tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
+    }
+  }
+  grid_dep_wait();
+  grid_dep_trigger();  // the dQ conversion may start launching (it waits for this kernel's results)
+
   if (warp == 12) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
-      tma_prefetch_desc(&tmap_do);
-      constexpr uint32_t tb = L::kTileBytes, hb = L::kHalfBytes;
-      mbar_arrive_expect_tx(&bars[BB_KV], 2 * tb + kColRec * 4);
-      for (int x = 0; x < D / 64; ++x) {
-        tma_load_4d(sm + L::kK + x * 16384, &tmap_k, &bars[BB_KV], x * 64, h, J * kTile, b);
-        tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
-      }
+      constexpr uint32_t hb = L::kHalfBytes;
       bulk_load(sm + L::kRec, p.colrec + ((size_t)bh * p.nT + J) * kColRec, kColRec * 4, &bars[BB_KV]);
       int fills[kStages] = {};
       for (int g = 0; g < G; ++g) {
@@ -761,6 +770,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(int B, int N, int H, int Npad, float scale,
                                                     const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq) {
+  grid_dep_trigger();  // the gate gradient may start launching
+  grid_dep_wait();     // the dQ accumulator of the attention kernel
   const long long blk = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const long long nblk = (long long)B * H * (Npad / 32) * (D / 32);
@@ -845,6 +856,7 @@ __global__ void __launch_bounds__(kGateThreads) gate_grad_kernel(int B, int N, i
   __shared__ float xs[kGateHeads][kTile + 1];               // [head][token]: R - C, then d a
   __shared__ float cs[kGateHeads][kTile + 1];               // C (bias_from_j)
   __shared__ unsigned s_ticket;
+  grid_dep_wait();  // R and C of the attention kernel; the ticket and status records the row kernel cleared
   if (threadIdx.x == 0) s_ticket = atomicAdd(ticket, 1u);
   __syncthreads();
   const int HG = (H + kGateHeads - 1) / kGateHeads;
@@ -1044,17 +1056,18 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("attn_bwd", s);
-    kernel<<<(unsigned)blocks, kBwdThreads, L::kAlloc, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    e = launch_dependent(kernel, dim3((unsigned)blocks), dim3(kBwdThreads), L::kAlloc, s, maps[0], maps[1], maps[2],
+                         maps[3], maps[4], maps[5], p);
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long dblocks = (long long)a.B * a.H * (g.Npad / 32) * (D / 32);  // 4 KB accumulator blocks
   {
     TraceScope trace("bwd_dq", s);
-    bwd_dq_kernel<D><<<(unsigned)((dblocks + 7) / 8), 256, 0, s>>>(a.B, a.N, a.H, g.Npad, a.scale, dqacc,
-                                                                 static_cast<__nv_bfloat16*>(a.dq));
+    e = launch_dependent(bwd_dq_kernel<D>, dim3((unsigned)((dblocks + 7) / 8)), dim3(256), 0, s, a.B, a.N, a.H,
+                         g.Npad, a.scale, (const float*)dqacc, static_cast<__nv_bfloat16*>(a.dq));
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_gate_bwd(a.B, a.N, a.H, g.Npad, a.bias_from_j, colsum, rowsum, a.z, a.dz, a.ws + w.gstat,
                          reinterpret_cast<unsigned*>(a.ws + kTicketOffset), err, s);
@@ -1072,8 +1085,10 @@ cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, co
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("bwd_gate", s);
-    gate_grad_kernel<<<(unsigned)ctas, kGateThreads, 0, s>>>(B, N, H, nT, stride, bias_from_j, colsum, rowsum, z, dz,
-                                                    static_cast<GateStat*>(stat), ticket, err);
+    const cudaError_t e = launch_dependent(gate_grad_kernel, dim3((unsigned)ctas), dim3(kGateThreads), 0, s, B, N, H,
+                                           nT, stride, bias_from_j, colsum, rowsum, z, dz,
+                                           static_cast<GateStat*>(stat), ticket, err);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(256) gate_tile_scan_kernel(const float* __rest
   __shared__ float zs[kTile][kHeadsPerPass + 1];
   const int T = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * kTileScanHeads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_trigger();  // the base scan may start launching (it waits for this kernel's results)
   if (T == 0 && b == 0 && h0 == 0 && threadIdx.x == 0 && err) *err = 0u;  // each call starts with a clean error word
   const int t0 = T * kTile;
   const int nh = min(kTileScanHeads, H - h0);
@@ -122,6 +123,7 @@ __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.syn
 __global__ void __launch_bounds__(kProjThreads, 1)
     gate_proj_scan_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                           const ProjParams p) {
+  grid_dep_trigger();  // the base scan may start launching (it waits for this kernel's results)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t xb = kTile * 64 * 2;            // x chunk bytes (16 KB)
@@ -264,6 +266,8 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
 // loaded before the scan (4 per lane), so the loads overlap.
 __global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, const float* __restrict__ tiletot,
                                                              float* __restrict__ colrec) {
+  grid_dep_trigger();  // the attention kernel may start its prologue
+  grid_dep_wait();     // the tile totals of the tile scan
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= BH) return;
   DF carry{0.f, 0.f};
@@ -337,9 +341,10 @@ cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const floa
   if (e != cudaSuccess) return e;
   {
     TraceScope trace("gate_base_scan", s);
-    gate_base_scan_kernel<<<(g.BH + 7) / 8, 256, 0, s>>>(g.BH, g.nT, p.tiletot, p.colrec);
+    e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + 7) / 8), dim3(256), 0, s, g.BH, g.nT,
+                         (const float*)p.tiletot, p.colrec);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 namespace {
@@ -389,9 +394,10 @@ cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_
   const int warps_per_block = 8;
   {
     TraceScope trace("gate_base_scan", s);
-    gate_base_scan_kernel<<<(g.BH + warps_per_block - 1) / warps_per_block, 256, 0, s>>>(g.BH, g.nT, tiletot, colrec);
+    e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + warps_per_block - 1) / warps_per_block), dim3(256), 0,
+                         s, g.BH, g.nT, (const float*)tiletot, colrec);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fox

@@ -109,6 +109,27 @@ struct TraceScope {
   ~TraceScope();
 };
 
+// Launch `kernel` on `s` as a programmatic dependent of the kernel launched just before it on
+// the same stream: it may start while that kernel still runs, so it must call grid_dep_wait()
+// (fox_ptx.cuh) before reading anything that kernel (or any earlier one) wrote. Its prologue
+// (barrier set-up, tensor-memory allocation, loads of the caller's inputs) then overlaps the
+// end of the kernel before it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers (return cudaGetLastError() of the launch) ----
 // c[b,t,h] = (base_T + local_t) / log2 e from the gate terms in the workspace (fp64 sum, fp32 out).
 cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, int N, int H, float* c, cudaStream_t s);

@@ -102,6 +102,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched as a programmatic dependent (launch_dependent in fox_internal.h) may start
+// while the kernel before it on the stream still runs: grid_dep_wait() blocks until that kernel
+// has completed and its memory operations are visible; nothing it wrote may be read before.
+// grid_dep_trigger() lets the kernel after this one start launching (it still waits for this
+// kernel's completion before reading its results). Both are no-ops without such a launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // --------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -846,7 +846,9 @@ constexpr int kGateHeads = 32;     // heads per gate-gradient CTA
 constexpr int kGateThreads = 512;  // 16 warps, two heads each
 constexpr int kLookLanes = 16;     // lanes (blocks read per round) of one head's look-back
 
-__global__ void __launch_bounds__(kGateThreads) gate_grad_kernel(int B, int N, int H, int nT, int stride,
+// Three CTAs per SM (40 registers, no spills): more blocks' loads in flight, since each CTA runs its
+// loads, look-back and stores in sequence (two per SM: 190 us on B64 H32 N16384, three: 173 us).
+__global__ void __launch_bounds__(kGateThreads, 3) gate_grad_kernel(int B, int N, int H, int nT, int stride,
                                                                  int bias_from_j, const float* __restrict__ colsum,
                                                                  const float* __restrict__ rowsum,
                                                                  const float* __restrict__ z, float* __restrict__ dz,

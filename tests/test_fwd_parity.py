@@ -144,6 +144,21 @@ def test_train_workload_forward_all_rows():
     check_all_rows(wl.TRAIN_BF16)
 
 
+@pytest.mark.parametrize("gate", ["open", "slow"])
+def test_row_maximum_growing_on_a_far_tile(gate):
+    """Keys 0..127 scaled by 8: their scores dwarf those near the diagonal, so for most rows the
+    maximum sits in the last key tile visited (tile 0; tiles are visited from the diagonal back)
+    and exceeds the running maximum by far more than the rescale threshold, so O and the row sum
+    are rescaled late in the row. Open gates (f = 1) and slowly forgetting ones (z ~ N(6, 1))."""
+    w = wl.Workload(f"grow_{gate}", 1, 900, 2, 128, "bf16", seed=71, gate="open" if gate == "open" else "normal",
+                    lo=6.0)
+    arrays = wl.draw(w)
+    k = wl.bf16_bits_to_f64(arrays["k"]).astype(np.float32)
+    k[:, :128] *= 8.0
+    arrays["k"] = wl.f32_to_bf16_bits(k).reshape(arrays["k"].shape)
+    check_full(w, arrays=arrays)
+
+
 def test_forward_is_deterministic():
     w = wl.Workload("det", 2, 700, 3, 128, "bf16", seed=9, gate="head_uniform", lo=0.0, hi=4.0)
     a, o1, l1 = run_fwd(w)

@@ -36,6 +36,7 @@ EXPORTS = (
     "fox_fwd",
     "fox_bwd",
     "fox_fwd_workspace_bytes",
+    "fox_fwd_min_workspace_bytes",
     "fox_bwd_workspace_bytes",
     "fox_check_error",
     "fox_status_string",
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
         L.fox_bwd.restype = i
         L.fox_fwd_workspace_bytes.argtypes = [pp]
         L.fox_fwd_workspace_bytes.restype = sz
+        L.fox_fwd_min_workspace_bytes.argtypes = [pp]
+        L.fox_fwd_min_workspace_bytes.restype = sz
         L.fox_bwd_workspace_bytes.argtypes = [pp]
         L.fox_bwd_workspace_bytes.restype = sz
         L.fox_check_error.argtypes = [vp, vp]
@@ -161,6 +164,10 @@ def make_params(B, N, H, d, dtype=FOX_DTYPE_BF16, scale=0.0, bias_from_j=False, 
 
 def fox_fwd_workspace_bytes(params: fox_params) -> int:
     return int(lib().fox_fwd_workspace_bytes(ctypes.byref(params)))
+
+
+def fox_fwd_min_workspace_bytes(params: fox_params) -> int:
+    return int(lib().fox_fwd_min_workspace_bytes(ctypes.byref(params)))
 
 
 def fox_bwd_workspace_bytes(params: fox_params) -> int:

@@ -32,7 +32,7 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows) {
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows, bool f16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
@@ -40,7 +40,8 @@ bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int 
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+             dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -167,9 +168,16 @@ const char* fox_status_string(fox_status s) {
   return "FOX_ERR_UNKNOWN";
 }
 
-size_t fox_fwd_workspace_bytes(const fox_params* p) {
+size_t fox_fwd_min_workspace_bytes(const fox_params* p) {
   if (check_params(p) != FOX_OK) return 0;
   return gate_layout(p->B, p->N, p->H).end;
+}
+
+size_t fox_fwd_workspace_bytes(const fox_params* p) {
+  if (check_params(p) != FOX_OK) return 0;
+  const GateLayout g = gate_layout(p->B, p->N, p->H);
+  if (p->dtype != FOX_DTYPE_BF16) return g.end;
+  return fwd_v16_offset(g) + fwd_v16_bytes(p->B, p->N, p->H, p->d);
 }
 
 size_t fox_bwd_workspace_bytes(const fox_params* p) {
@@ -182,10 +190,18 @@ size_t fox_bwd_workspace_bytes(const fox_params* p) {
 
 namespace {
 
-// The forward after the gate terms are in the workspace: tile spans (tile_skip), then the
-// attention kernel.
+// Where the forward's fp16 copy of V goes (bf16 with a workspace that has room for it), or null:
+// the attention kernel then converts each V tile on chip.
+void* fwd_v16_slot(const fox_params* p, void* workspace, size_t workspace_bytes, const GateLayout& g) {
+  if (p->dtype != FOX_DTYPE_BF16) return nullptr;
+  if (workspace_bytes < fwd_v16_offset(g) + fwd_v16_bytes(p->B, p->N, p->H, p->d)) return nullptr;
+  return static_cast<char*>(workspace) + fwd_v16_offset(g);
+}
+
+// The forward after the gate terms (and the fp16 copy of V, when v16 is set) are in the
+// workspace: tile spans (tile_skip), then the attention kernel.
 fox_status fwd_after_gate(const fox_params* p, const void* q, const void* k, const void* v, void* o, float* lse,
-                          void* workspace, const GateLayout& g, cudaStream_t s) {
+                          void* workspace, const void* v16, const GateLayout& g, cudaStream_t s) {
   if (p->tile_skip &&
       launch_tile_span(q, k, p->B, p->N, p->H, p->d, effective_scale(p), g, workspace, s) != cudaSuccess)
     return FOX_ERR_CUDA;
@@ -211,16 +227,18 @@ fox_status fwd_after_gate(const fox_params* p, const void* q, const void* k, con
     if (p->B * p->H > 65535) return FOX_ERR_UNSUPPORTED;
     return launch_attn_fwd_f32(a, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
   }
+  a.v16 = v16;
   CUtensorMap maps[3];
   if (!make_bnhd_map(&maps[0], q, p->B, p->N, p->H, p->d) || !make_bnhd_map(&maps[1], k, p->B, p->N, p->H, p->d) ||
-      !make_bnhd_map(&maps[2], v, p->B, p->N, p->H, p->d))
+      !make_bnhd_map(&maps[2], a.v16 ? a.v16 : v, p->B, p->N, p->H, p->d, kTile, a.v16 != nullptr))
     return FOX_ERR_CUDA;
   return launch_attn_fwd_bf16(a, maps, g.nT, g.Npad, s) == cudaSuccess ? FOX_OK : FOX_ERR_CUDA;
 }
 
 // Checks and the fused projection + scan shared by fox_gate_proj and fox_fwd_xgate.
 fox_status gate_proj(const fox_params* p, int hidden, const void* x, const void* w_f, const float* b_f, float* z,
-                     void* workspace, size_t workspace_bytes, const GateLayout& g, cudaStream_t s) {
+                     void* workspace, size_t workspace_bytes, const GateLayout& g, cudaStream_t s,
+                     const V16Job* v16 = nullptr) {
   if (p->dtype != FOX_DTYPE_BF16) return FOX_ERR_UNSUPPORTED;
   if (hidden <= 0 || hidden % 8 != 0) return FOX_ERR_INVALID_ARG;
   if (p->H > 256) return FOX_ERR_UNSUPPORTED;
@@ -231,7 +249,7 @@ fox_status gate_proj(const fox_params* p, int hidden, const void* x, const void*
   if (st != FOX_OK) return st;
   CUtensorMap maps[2];
   if (!make_x_map(&maps[0], x, p->B, p->N, hidden) || !make_wf_map(&maps[1], w_f, p->H, hidden)) return FOX_ERR_CUDA;
-  return launch_gate_proj_scan(maps, b_f, hidden, z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) ==
+  return launch_gate_proj_scan(maps, b_f, hidden, z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s, v16) ==
                  cudaSuccess
              ? FOX_OK
              : FOX_ERR_CUDA;
@@ -254,8 +272,11 @@ fox_status fox_fwd(const fox_params* p, const void* q, const void* k, const void
   st = check_workspace(workspace, workspace_bytes, g.end);
   if (st != FOX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s) != cudaSuccess) return FOX_ERR_CUDA;
-  return fwd_after_gate(p, q, k, v, o, lse, workspace, g, s);
+  void* v16 = fwd_v16_slot(p, workspace, workspace_bytes, g);
+  const V16Job job{v, v16, fwd_v16_bytes(p->B, p->N, p->H, p->d) / 2};
+  if (launch_gate_scan(z, p->B, p->N, p->H, p->bias_from_j, workspace, g, s, v16 ? &job : nullptr) != cudaSuccess)
+    return FOX_ERR_CUDA;
+  return fwd_after_gate(p, q, k, v, o, lse, workspace, v16, g, s);
 }
 
 fox_status fox_gate_proj(const fox_params* p, int hidden, const void* x, const void* w_f, const float* b_f, float* z,
@@ -279,9 +300,11 @@ fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const v
     return FOX_ERR_INVALID_ARG;
   const GateLayout g = gate_layout(p->B, p->N, p->H);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = gate_proj(p, hidden, x, w_f, b_f, z, workspace, workspace_bytes, g, s);
+  void* v16 = fwd_v16_slot(p, workspace, workspace_bytes, g);
+  const V16Job job{v, v16, fwd_v16_bytes(p->B, p->N, p->H, p->d) / 2};
+  st = gate_proj(p, hidden, x, w_f, b_f, z, workspace, workspace_bytes, g, s, v16 ? &job : nullptr);
   if (st != FOX_OK) return st;
-  return fwd_after_gate(p, q, k, v, o, lse, workspace, g, s);
+  return fwd_after_gate(p, q, k, v, o, lse, workspace, v16, g, s);
 }
 
 fox_status fox_bwd(const fox_params* p, const void* q, const void* k, const void* v, const float* z, const void* o,

@@ -27,6 +27,8 @@
 //   warp  8    TMA producer (Q once; K, V and the column-term record per KV tile, 2 stages)
 //   warp  9    TMEM allocator and single-thread MMA issuer
 //   warps 10-11 V converters: each V tile from bf16 to fp16, in place in shared memory
+//               (only when V is not already in fp16: the caller's workspace normally holds
+//               an fp16 copy, written once by v_to_f16_kernel, and these warps do not exist)
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
 // P (fp16) overwrites the first 64 columns of its S buffer and feeds the P V
 // MMA straight from tensor memory.
@@ -49,7 +51,8 @@ namespace {
 
 constexpr int kConvWarps = 2;  // V converter warps (one measured 21 % slower on the long workload, three or
                                // four 9-11 %: their threads lower the register cap of every warp to 128)
-constexpr int kThreads = 320 + 32 * kConvWarps;
+// Threads: with V in fp16 already (kPreV) there are no converter warps.
+__host__ __device__ constexpr int fwd_threads(bool pre_v) { return 320 + (pre_v ? 0 : 32 * kConvWarps); }
 constexpr int kKappaBytes = kColRec * 4;   // 528
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum while the tile max stays within 2^8
 
@@ -216,8 +219,8 @@ struct StageC {
   static constexpr int value = V;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kPreV>
+__global__ void __launch_bounds__(fwd_threads(kPreV), 1)
     fox_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const FwdKParams p) {
   using L = FwdLayout<D>;
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_SFULL + s], 1);
       mbar_init(&bars[B_PFULL + s], 4);
       mbar_init(&bars[B_OFINAL + s], 1);
-      mbar_init(&bars[B_VCONV + s], kConvWarps);
+      if (!kPreV) mbar_init(&bars[B_VCONV + s], kConvWarps);
     }
     mbar_init(&bars[B_DONE], 1);
     *abort_flag = 0;
@@ -326,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t tb = L::kTileBytes;
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_f16(128, D, false, true);  // P (TMEM) and V fp16
+      // V of a stage is ready for P V once it landed (kPreV: loaded as fp16) or was converted.
+      constexpr uint32_t kVErr = kPreV ? DEV_ERR_TIMEOUT_TMA : DEV_ERR_TIMEOUT_SYNC;
       const uint32_t tS[2] = {tbase, tbase + 128};
       const uint32_t tO[2] = {tbase + 256, tbase + 256 + D};
       // Descriptors of each operand tile's base. Shared-memory addresses stay below 2^18, so
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // on the stage parity so that every descriptor and barrier address is fixed.
         auto straight = [&](auto stage) -> bool {
           constexpr int ST = decltype(stage)::value, NST = ST ^ 1;
-          bool ok = mbar_wait(&bars[B_VCONV + ST], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC) &&
+          bool ok = mbar_wait(&bars[(kPreV ? B_VFULL : B_VCONV) + ST], (s >> 1) & 1, abort_flag, p.err, kVErr) &&
                     mbar_wait(&bars[B_PFULL + 0], (s - first0) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) return false;
           tc_fence_after();
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           continue;
         }
-        ok = mbar_wait(&bars[B_VCONV + st], (s >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
+        ok = mbar_wait(&bars[(kPreV ? B_VFULL : B_VCONV) + st], (s >> 1) & 1, abort_flag, p.err, kVErr);
         for (int k = 0; k < 2 && ok; ++k) {
           if (!active[k]) continue;
           if (s >= first[k] && s < end[k]) {
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bars[B_DONE], 0);
     }
     __syncwarp();
-  } else if (warp >= 10) {
+  } else if (!kPreV && warp >= 10) {
     // ----------------------------------------------------------- V converters
     // Each V tile in place from bf16 to fp16, the two warps taking alternate 16-byte pieces
     // of the swizzled layout TMA wrote (the conversion is per element, so the layout is
@@ -611,11 +616,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+// V (bf16 bits) to fp16, 16-byte pieces in a grid-stride loop with four loads in flight per
+// thread. Every bf16 value of magnitude 2^-14 .. 65280 is exactly an fp16 value; smaller ones
+// round to the nearest multiple of 2^-24 (cvt.rn); 65536 and above (infinities included) are
+// outside fp16 and set DEV_ERR_RANGE. The error word is cleared by the gate scan that runs
+// before this kernel, so the bit is set only after grid_dep_wait(), which also makes this
+// kernel end after the one before it (the attention kernel waits on this one alone).
+constexpr int kV16Threads = 256;
+constexpr int kV16Unroll = 4;
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, uint32_t& vmax) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[q] = pack_f16x2(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(vmax) : "r"(in[q] & 0x7FFF7FFFu));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __launch_bounds__(kV16Threads) v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16,
+                                                                size_t pieces, uint32_t* err) {
+  grid_dep_trigger();  // the attention kernel may start launching (it waits for this one)
+  uint32_t vmax = 0u;
+  const size_t stride = (size_t)gridDim.x * kV16Threads;
+  size_t i = (size_t)blockIdx.x * kV16Threads + threadIdx.x;
+  for (; i + (kV16Unroll - 1) * stride < pieces; i += kV16Unroll * stride) {
+    uint4 w[kV16Unroll];
+#pragma unroll
+    for (int u = 0; u < kV16Unroll; ++u) w[u] = __ldcs(v + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kV16Unroll; ++u) v16[i + u * stride] = bf16x8_to_f16x8(w[u], vmax);
+  }
+  for (; i < pieces; i += stride) v16[i] = bf16x8_to_f16x8(__ldcs(v + i), vmax);
+  const bool over = (vmax & 0xFFFFu) >= 0x4780u || (vmax >> 16) >= 0x4780u;
+  grid_dep_wait();
+  if (__any_sync(0xffffffffu, over) && (threadIdx.x & 31) == 0) atomicOr(err, DEV_ERR_RANGE);
+}
+
+template <int D, bool kPreV>
 cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
   using L = FwdLayout<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  auto kernel = fox_attn_fwd_kernel<D>;
+  auto kernel = fox_attn_fwd_kernel<D, kPreV>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdKParams p;
@@ -637,7 +681,7 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   {
     TraceScope trace("attn_fwd", s);
-    e = launch_dependent(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), L::kAlloc, s, maps[0], maps[1],
+    e = launch_dependent(kernel, dim3(static_cast<unsigned>(blocks)), dim3(fwd_threads(kPreV)), L::kAlloc, s, maps[0], maps[1],
                          maps[2], p);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -646,9 +690,23 @@ cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int 
 }  // namespace
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
-  if (a.d == 64) return launch_d<64>(a, maps, nT, Npad, s);
-  if (a.d == 128) return launch_d<128>(a, maps, nT, Npad, s);
+  if (a.d == 64) return a.v16 ? launch_d<64, true>(a, maps, nT, Npad, s) : launch_d<64, false>(a, maps, nT, Npad, s);
+  if (a.d == 128) return a.v16 ? launch_d<128, true>(a, maps, nT, Npad, s) : launch_d<128, false>(a, maps, nT, Npad, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_v_to_f16(const void* v, void* v16, size_t n, uint32_t* err, cudaStream_t s) {
+  const size_t pieces = n / 8;
+  if (pieces == 0) return cudaSuccess;
+  size_t blocks = (pieces + kV16Threads * kV16Unroll - 1) / (kV16Threads * kV16Unroll);
+  if (blocks > 4096) blocks = 4096;  // a grid-stride loop covers the rest
+  cudaError_t e;
+  {
+    TraceScope trace("v_f16", s);
+    e = launch_dependent(v_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kV16Threads), 0, s,
+                         static_cast<const uint4*>(v), static_cast<uint4*>(v16), pieces, err);
+  }
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fox

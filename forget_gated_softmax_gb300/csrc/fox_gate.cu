@@ -310,7 +310,7 @@ size_t gate_proj_smem_bytes(int H) {
 
 cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const float* bias, int hidden, float* z_out,
                                   int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const V16Job* v16) {
   char* base = static_cast<char*>(ws);
   uint32_t* err = reinterpret_cast<uint32_t*>(base);
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);  // each call starts with a clean error word
@@ -339,6 +339,7 @@ cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const floa
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (v16 && (e = launch_v_to_f16(v16->v, v16->v16, v16->n, err, s)) != cudaSuccess) return e;
   {
     TraceScope trace("gate_base_scan", s);
     e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + 7) / 8), dim3(256), 0, s, g.BH, g.nT,
@@ -378,7 +379,7 @@ cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, i
 }
 
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
-                             cudaStream_t s) {
+                             cudaStream_t s, const V16Job* v16) {
   char* base = static_cast<char*>(ws);
   float* rowloc = reinterpret_cast<float*>(base + g.rowloc);
   float* colrec = reinterpret_cast<float*>(base + g.colrec);
@@ -391,6 +392,8 @@ cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // The forward's V conversion runs alongside the tile scan; the base scan waits for both.
+  if (v16 && (e = launch_v_to_f16(v16->v, v16->v16, v16->n, err, s)) != cudaSuccess) return e;
   const int warps_per_block = 8;
   {
     TraceScope trace("gate_base_scan", s);

@@ -139,8 +139,14 @@ cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, i
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
                             const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
                             uint32_t* err, cudaStream_t s);
+// V (bf16, n elements) to fp16 into v16, run between the two gate kernels (see launch_v_to_f16).
+struct V16Job {
+  const void* v;
+  void* v16;
+  size_t n;
+};
 cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_j, void* ws, const GateLayout& g,
-                             cudaStream_t s);
+                             cudaStream_t s, const V16Job* v16 = nullptr);
 
 struct AttnFwdArgs {
   int B, N, H, d;
@@ -155,9 +161,20 @@ struct AttnFwdArgs {
   const float* colrec;
   uint32_t* err;
   const int* jmin = nullptr;  // tile skipping: first key tile of each query tile ([bh][nT]), or null
+  const void* v16 = nullptr;  // fp16 copy of v ([B, N, H, d]), or null: the kernel then converts V on chip
 };
 
-cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v */, int nT, int Npad,
+// The forward's fp16 copy of V sits after the gate terms: B N H d halves.
+inline size_t fwd_v16_offset(const GateLayout& g) { return g.end; }
+inline size_t fwd_v16_bytes(int B, int N, int H, int d) { return (size_t)B * N * H * d * 2; }
+
+// V (bf16, n elements, a multiple of 8, 16-byte aligned) to fp16; a magnitude of 65536 or
+// more (outside fp16) sets DEV_ERR_RANGE in err. Launched as a programmatic dependent of the
+// gate tile scan (which clears err), so that the two run at once; it awaits that kernel's
+// completion before it ends, and the base scan after it waits for it in turn.
+cudaError_t launch_v_to_f16(const void* v, void* v16, size_t n, uint32_t* err, cudaStream_t s);
+
+cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v (v16 when set) */, int nT, int Npad,
                                  cudaStream_t s);
 cudaError_t launch_attn_fwd_f32(const AttnFwdArgs& a, int nT, int Npad, cudaStream_t s);
 
@@ -210,7 +227,8 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a, const GateLayout& g, const Bwd
 // maps: x as [B, N, hidden] (box 64 x 128 x 1), W_f as [H, hidden] (box 64 x Hpad), both bf16,
 // 128-byte swizzle; H <= 256.
 cudaError_t launch_gate_proj_scan(const CUtensorMap* maps, const float* bias, int hidden, float* z_out, int B, int N,
-                                  int H, int bias_from_j, void* ws, const GateLayout& g, cudaStream_t s);
+                                  int H, int bias_from_j, void* ws, const GateLayout& g, cudaStream_t s,
+                                  const V16Job* v16 = nullptr);
 
 // Decay-aware tile skipping: per-tile norms of q and k, then the key-tile span of every
 // query tile (jmin) and the query-tile span of every key tile (imax); needs the gate scan.
@@ -224,7 +242,8 @@ size_t window_workspace_bytes(int B, int N, int H);
 // Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 channels x 1 head x
 // box_rows tokens x 1 batch and 128-byte swizzle. Returns false when the driver entry point is
 // unavailable or encoding fails.
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows = kTile);
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows = kTile,
+                   bool f16 = false);
 // Host helpers for the gate projection: x [B, N, hidden] with a box of 64 x 128 x 1, and
 // W_f [H, hidden] with a box of 64 x (H rounded up to 16); bf16, 128-byte swizzle.
 bool make_x_map(CUtensorMap* map, const void* base, int B, int N, int hidden);

@@ -4,7 +4,8 @@
 // run this library: a plugin inside a host application that owns all device
 // memory and does not let its plugins allocate, or a latency-bound loop that
 // cannot afford an allocation's implicit synchronisation. fox_fwd needs a
-// caller-provided workspace for the gate terms; this entry point instead uses
+// caller-provided workspace for the gate terms (and, when it has room, an fp16
+// copy of V); this entry point instead uses
 // a fixed scratch array compiled into the library (kStaticScratchBytes, held
 // by every GPU that loads the library until the process exits). The caller
 // still passes inputs and outputs.
@@ -69,7 +70,8 @@ fox_status fox_noalloc_check_error(void* stream) {
 fox_status fox_fwd_noalloc(const fox_params* p, const void* q, const void* k, const void* v, const float* z, void* o,
                            float* lse, void* stream) {
   if (!p) return FOX_ERR_INVALID_ARG;
-  const size_t need = fox_fwd_workspace_bytes(p);
+  // The gate terms must fit; the fp16 copy of V is used when it fits too (fox_fwd decides by size).
+  const size_t need = fox_fwd_min_workspace_bytes(p);
   if (need == 0) return fox_fwd(p, q, k, v, z, o, lse, nullptr, 0, stream);  // reports the parameter error
   if (need > kStaticScratchBytes) return FOX_ERR_WORKSPACE;                  // larger than the fixed scratch
   if (p->B == 0 || p->H == 0 || p->N == 0) return FOX_OK;

@@ -90,8 +90,17 @@ typedef struct fox_params {
                       results are wrong (nothing faults: every index comes from B, N, H). */
 } fox_params;
 
-/* Workspace bytes fox_fwd / fox_bwd need for these params (0 if params are invalid). */
+/*
+ * Workspace bytes for these params (0 if params are invalid).
+ * fox_fwd_workspace_bytes: the gate terms plus, for bf16, an fp16 copy of V
+ *   (B*N*H*d*2 bytes), which fox_fwd writes once and the attention kernel reads.
+ * fox_fwd_min_workspace_bytes: the gate terms alone, the least fox_fwd accepts.
+ *   With less than fox_fwd_workspace_bytes the attention kernel converts every
+ *   V tile it loads on chip instead (same results, bit for bit; slower).
+ * fox_bwd_workspace_bytes: everything fox_bwd needs (more than the forward's).
+ */
 size_t fox_fwd_workspace_bytes(const fox_params* p);
+size_t fox_fwd_min_workspace_bytes(const fox_params* p);
 size_t fox_bwd_workspace_bytes(const fox_params* p);
 
 /*
@@ -99,10 +108,12 @@ size_t fox_bwd_workspace_bytes(const fox_params* p);
  * allowed and means f = 1; -inf and NaN are outside the domain). Writes
  * O [B,N,H,d] (params.dtype; bf16 rounded to nearest even) and
  * LSE [B,N,H] (fp32, natural log, bias included).
- * Steps: gate log-sigmoid + per-head prefix scan into the workspace, then the
- * fused causal attention kernel. B*H == 0 or N == 0 returns FOX_OK with no work.
+ * Steps: gate log-sigmoid + per-head prefix scan into the workspace, V to fp16
+ * into the workspace (when it has room, see above), then the fused causal
+ * attention kernel. B*H == 0 or N == 0 returns FOX_OK with no work.
+ * Workspace: at least fox_fwd_min_workspace_bytes(p), else FOX_ERR_WORKSPACE.
  * Precision (bf16): S = Q K^T in bf16 with fp32 accumulation, the softmax in
- * fp32, and P V in fp16 (P and V converted to fp16 on chip, fp32 accumulation),
+ * fp32, and P V in fp16 (P on chip and V converted to fp16, fp32 accumulation),
  * so that the weights carry 11 significant bits instead of bf16's 8. Every bf16
  * V value of magnitude 2^-14 .. 65280 converts exactly; smaller ones round to a
  * multiple of 2^-24; a V value of magnitude 65536 or more sets a device error
@@ -235,8 +246,9 @@ fox_status fox_tile_span(const fox_params* p, const void* q, const void* k, cons
  * Same arguments and results as fox_fwd, minus the workspace: the scratch
  * for the gate terms is a fixed array of fox_noalloc_scratch_bytes() (16 MiB)
  * compiled into the library, which every GPU that loads the library holds
- * until the process exits. Problems whose fox_fwd_workspace_bytes exceeds it
- * return FOX_ERR_WORKSPACE without touching the GPU. Allocates nothing
+ * until the process exits. Problems whose fox_fwd_min_workspace_bytes exceeds
+ * it return FOX_ERR_WORKSPACE without touching the GPU; the fp16 copy of V is
+ * used when fox_fwd_workspace_bytes fits too. Allocates nothing
  * (no cudaMalloc, cudaFree or allocating library call). The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture. All calls

@@ -63,6 +63,17 @@ def test_workspace_queries(L):
     assert big >= 32 * 16384 * 4 * 2
     assert fox.fox_fwd_workspace_bytes(_p(d=96)) == 0
     assert fox.fox_fwd_workspace_bytes(_p(N=-1)) == 0
+    assert fox.fox_fwd_min_workspace_bytes(_p(d=96)) == 0
+
+
+def test_forward_workspace_holds_the_gate_terms_then_an_fp16_copy_of_v(L):
+    for kw in (dict(), dict(B=3, N=700, H=5, d=128), dict(B=1, H=32, N=16384, d=128)):
+        p = _p(**kw)
+        lo, hi = fox.fox_fwd_min_workspace_bytes(p), fox.fox_fwd_workspace_bytes(p)
+        assert lo % 256 == 0 and hi - lo == p.B * p.N * p.H * p.d * 2
+    p = _p(dtype=1)  # the fp32 forward has no fp16 copy
+    assert fox.fox_fwd_min_workspace_bytes(p) == fox.fox_fwd_workspace_bytes(p) > 0
+    assert _fwd(L, _p(), nbytes=fox.fox_fwd_min_workspace_bytes(_p()) - 1) == 3
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first

@@ -56,16 +56,19 @@ def test_context_stays_usable_after_a_timeout():
     assert torch.equal(l0.view(torch.int32), l1.view(torch.int32))
 
 
-def test_v_outside_fp16_range_is_reported():
+@pytest.mark.parametrize("path", ["fp16 copy", "on chip"])
+def test_v_outside_fp16_range_is_reported(path):
     """The forward's P V runs in fp16: a V value of magnitude 65536 or more cannot be held
-    there, and the converter reports it as FOX_ERR_DEVICE (the other outputs are then not
-    meaningful; nothing faults)."""
+    there, and the conversion reports it as FOX_ERR_DEVICE (the other outputs are then not
+    meaningful; nothing faults), whether V is converted into the workspace (a workspace of
+    fox_fwd_workspace_bytes) or tile by tile in the attention kernel (the minimum workspace)."""
     import forget_gated_softmax_gb300 as fox
 
     w = wl.Workload("vrange", 1, 300, 2, 64, "bf16", seed=6, gate="normal", lo=1.0)
     t = to_torch(wl.draw(w), "bf16")
     p = fox.make_params(w.B, w.N, w.H, w.d)
-    ws = fox.workspace(fox.fox_fwd_workspace_bytes(p), "cuda")
+    nbytes = fox.fox_fwd_workspace_bytes(p) if path == "fp16 copy" else fox.fox_fwd_min_workspace_bytes(p)
+    ws = fox.workspace(nbytes, "cuda")[:nbytes]
     fox.fox_fwd(t["q"], t["k"], t["v"], t["z"], ws=ws)
     assert fox.fox_check_error(ws) == 0
     v = t["v"].clone()

@@ -421,7 +421,8 @@ def run_fox(args, rank: int, world: int, local_rank: int):
         "attn_bwd": ("tensor", w.bwd_flops()),
         "gate_tile_scan": ("hbm", w.tokens * (4 + 4 + 4 + 4)),   # z in; rowloc, colrec, tile totals out
         "gate_base_scan": ("hbm", w.B * w.H * ((w.N + 127) // 128) * (4 + 16)),
-        "v_f16": ("hbm", w.tokens * w.d * (2 + 2)),  # V (bf16) in, its fp16 copy out
+        # the base scan with the forward's fp16 copy of V: V (bf16) in, the copy out
+        "gate_base_scan_v16": ("hbm", w.tokens * w.d * (2 + 2) + w.B * w.H * ((w.N + 127) // 128) * (4 + 16)),
         "dq_zero": ("hbm", w.tokens * 4 * w.d),  # the dQ accumulator cleared (a stream-ordered memset)
         "bwd_rows": ("hbm", w.tokens * (2 * w.d * 2 + 4 + 4 + 4 + 4 + 4)),  # O, dO, lse, rowloc in; delta, rho, R out
         "bwd_dq": ("hbm", w.tokens * w.d * (4 + 2)),

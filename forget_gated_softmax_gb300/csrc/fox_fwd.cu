@@ -28,7 +28,8 @@
 //   warp  9    TMEM allocator and single-thread MMA issuer
 //   warps 10-11 V converters: each V tile from bf16 to fp16, in place in shared memory
 //               (only when V is not already in fp16: the caller's workspace normally holds
-//               an fp16 copy, written once by v_to_f16_kernel, and these warps do not exist)
+//               an fp16 copy, written once by the gate step's base-scan kernel, and these
+//               warps do not exist)
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0, O1 (d columns each).
 // P (fp16) overwrites the first 64 columns of its S buffer and feeds the P V
 // MMA straight from tensor memory.
@@ -616,45 +617,6 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
   }
 }
 
-// V (bf16 bits) to fp16, 16-byte pieces in a grid-stride loop with four loads in flight per
-// thread. Every bf16 value of magnitude 2^-14 .. 65280 is exactly an fp16 value; smaller ones
-// round to the nearest multiple of 2^-24 (cvt.rn); 65536 and above (infinities included) are
-// outside fp16 and set DEV_ERR_RANGE. The error word is cleared by the gate scan that runs
-// before this kernel, so the bit is set only after grid_dep_wait(), which also makes this
-// kernel end after the one before it (the attention kernel waits on this one alone).
-constexpr int kV16Threads = 256;
-constexpr int kV16Unroll = 4;
-
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, uint32_t& vmax) {
-  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-  uint32_t out[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    out[q] = pack_f16x2(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(vmax) : "r"(in[q] & 0x7FFF7FFFu));
-  }
-  return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
-__global__ void __launch_bounds__(kV16Threads) v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16,
-                                                                size_t pieces, uint32_t* err) {
-  grid_dep_trigger();  // the attention kernel may start launching (it waits for this one)
-  uint32_t vmax = 0u;
-  const size_t stride = (size_t)gridDim.x * kV16Threads;
-  size_t i = (size_t)blockIdx.x * kV16Threads + threadIdx.x;
-  for (; i + (kV16Unroll - 1) * stride < pieces; i += kV16Unroll * stride) {
-    uint4 w[kV16Unroll];
-#pragma unroll
-    for (int u = 0; u < kV16Unroll; ++u) w[u] = __ldcs(v + i + u * stride);
-#pragma unroll
-    for (int u = 0; u < kV16Unroll; ++u) v16[i + u * stride] = bf16x8_to_f16x8(w[u], vmax);
-  }
-  for (; i < pieces; i += stride) v16[i] = bf16x8_to_f16x8(__ldcs(v + i), vmax);
-  const bool over = (vmax & 0xFFFFu) >= 0x4780u || (vmax >> 16) >= 0x4780u;
-  grid_dep_wait();
-  if (__any_sync(0xffffffffu, over) && (threadIdx.x & 31) == 0) atomicOr(err, DEV_ERR_RANGE);
-}
-
 template <int D, bool kPreV>
 cudaError_t launch_d(const AttnFwdArgs& a, const CUtensorMap* maps, int nT, int Npad, cudaStream_t s) {
   using L = FwdLayout<D>;
@@ -693,20 +655,6 @@ cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps, 
   if (a.d == 64) return a.v16 ? launch_d<64, true>(a, maps, nT, Npad, s) : launch_d<64, false>(a, maps, nT, Npad, s);
   if (a.d == 128) return a.v16 ? launch_d<128, true>(a, maps, nT, Npad, s) : launch_d<128, false>(a, maps, nT, Npad, s);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_v_to_f16(const void* v, void* v16, size_t n, uint32_t* err, cudaStream_t s) {
-  const size_t pieces = n / 8;
-  if (pieces == 0) return cudaSuccess;
-  size_t blocks = (pieces + kV16Threads * kV16Unroll - 1) / (kV16Threads * kV16Unroll);
-  if (blocks > 4096) blocks = 4096;  // a grid-stride loop covers the rest
-  cudaError_t e;
-  {
-    TraceScope trace("v_f16", s);
-    e = launch_dependent(v_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kV16Threads), 0, s,
-                         static_cast<const uint4*>(v), static_cast<uint4*>(v16), pieces, err);
-  }
-  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fox

@@ -261,22 +261,18 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   return DF{hi, e - (hi - s)};
 }
 
-// One warp per (b, h): exclusive scan of the tile totals -> base_T, in double-float,
+// One warp, one (b, h): exclusive scan of the tile totals -> base_T, in double-float,
 // stored as the hi/lo pair in each column record. The totals of up to 128 tiles are
 // loaded before the scan (4 per lane), so the loads overlap.
-__global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, const float* __restrict__ tiletot,
-                                                             float* __restrict__ colrec) {
-  grid_dep_trigger();  // the attention kernel may start its prologue
-  grid_dep_wait();     // the tile totals of the tile scan
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= BH) return;
+__device__ __forceinline__ void base_scan_warp(size_t bh, int nT, int lane, const float* __restrict__ tiletot,
+                                               float* __restrict__ colrec) {
   DF carry{0.f, 0.f};
   for (int T0 = 0; T0 < nT; T0 += 128) {
     float v[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int T = T0 + 32 * q + lane;
-      v[q] = T < nT ? tiletot[(size_t)warp * nT + T] : 0.f;
+      v[q] = T < nT ? tiletot[(size_t)bh * nT + T] : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -292,12 +288,89 @@ __global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, con
       if (lane == 0) below = DF{0.f, 0.f};
       const DF base = df_add(carry, below);
       if (T < nT) {
-        float* rec = colrec + ((size_t)warp * nT + T) * kColRec;
+        float* rec = colrec + ((size_t)bh * nT + T) * kColRec;
         *reinterpret_cast<float4*>(rec + kTile) = make_float4(base.hi, base.lo, 0.f, 0.f);
       }
       carry = df_add(carry, DF{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)});
     }
   }
+}
+
+__global__ void __launch_bounds__(256) gate_base_scan_kernel(int BH, int nT, const float* __restrict__ tiletot,
+                                                             float* __restrict__ colrec) {
+  grid_dep_trigger();  // the attention kernel may start its prologue
+  grid_dep_wait();     // the tile totals of the tile scan
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp < BH) base_scan_warp((size_t)warp, nT, lane, tiletot, colrec);
+}
+
+// The forward's fp16 copy of V (the P V operand type) and the base scan in one kernel, run
+// as a programmatic dependent of the tile scan: V is converted while the tile scan runs; then
+// every warp waits for the tile scan and takes its share of the (b, h) base scans. V (bf16
+// bits) goes to fp16 in 16-byte pieces, a grid-stride loop with four loads in flight per
+// thread. Every bf16 value of magnitude 2^-14 .. 65280 is exactly an fp16 value; smaller ones
+// round to the nearest multiple of 2^-24 (cvt.rn); 65536 and above (infinities included) are
+// outside fp16 and set DEV_ERR_RANGE, after the wait (the tile scan, or the memset before the
+// fused projection, clears the error word first).
+constexpr int kV16Threads = 256;
+constexpr int kV16Unroll = 4;
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, uint32_t& vmax) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[q] = pack_f16x2(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(vmax) : "r"(in[q] & 0x7FFF7FFFu));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __launch_bounds__(kV16Threads) gate_base_scan_v16_kernel(int BH, int nT, const float* __restrict__ tiletot,
+                                                                          float* __restrict__ colrec,
+                                                                          const uint4* __restrict__ v,
+                                                                          uint4* __restrict__ v16, size_t pieces,
+                                                                          uint32_t* err) {
+  grid_dep_trigger();  // the attention kernel may start launching (it waits for this one)
+  uint32_t vmax = 0u;
+  const size_t stride = (size_t)gridDim.x * kV16Threads;
+  size_t i = (size_t)blockIdx.x * kV16Threads + threadIdx.x;
+  for (; i + (kV16Unroll - 1) * stride < pieces; i += kV16Unroll * stride) {
+    uint4 w[kV16Unroll];
+#pragma unroll
+    for (int u = 0; u < kV16Unroll; ++u) w[u] = __ldcs(v + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kV16Unroll; ++u) v16[i + u * stride] = bf16x8_to_f16x8(w[u], vmax);
+  }
+  for (; i < pieces; i += stride) v16[i] = bf16x8_to_f16x8(__ldcs(v + i), vmax);
+  const bool over = (vmax & 0xFFFFu) >= 0x4780u || (vmax >> 16) >= 0x4780u;
+  grid_dep_wait();  // the tile scan's totals and its clearing of the error word
+  const int lane = threadIdx.x & 31;
+  if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(err, DEV_ERR_RANGE);
+  const int warps = gridDim.x * (kV16Threads / 32);
+  for (int w = (int)((blockIdx.x * kV16Threads + threadIdx.x) >> 5); w < BH; w += warps)
+    base_scan_warp((size_t)w, nT, lane, tiletot, colrec);
+}
+
+// Launches the base scan after a tile-scan kernel: alone, or with the V conversion.
+cudaError_t launch_base_scan(const GateLayout& g, const float* tiletot, float* colrec, uint32_t* err,
+                             const V16Job* v16, cudaStream_t s) {
+  cudaError_t e;
+  if (!v16) {
+    TraceScope trace("gate_base_scan", s);
+    e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + 7) / 8), dim3(256), 0, s, g.BH, g.nT, tiletot, colrec);
+  } else {
+    const size_t pieces = v16->n / 8;
+    size_t blocks = (pieces + kV16Threads * kV16Unroll - 1) / (kV16Threads * kV16Unroll);
+    const size_t scan_blocks = ((size_t)g.BH + 7) / 8;
+    if (blocks < scan_blocks) blocks = scan_blocks;
+    if (blocks > 4096) blocks = 4096;  // grid-stride loops cover the rest
+    TraceScope trace("gate_base_scan_v16", s);
+    e = launch_dependent(gate_base_scan_v16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kV16Threads), 0, s,
+                         g.BH, g.nT, tiletot, colrec, static_cast<const uint4*>(v16->v), static_cast<uint4*>(v16->v16),
+                         pieces, err);
+  }
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -339,13 +412,7 @@ cudaError_t launch_gate_proj_scan(const CUtensorMap* maps /* x, W */, const floa
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (v16 && (e = launch_v_to_f16(v16->v, v16->v16, v16->n, err, s)) != cudaSuccess) return e;
-  {
-    TraceScope trace("gate_base_scan", s);
-    e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + 7) / 8), dim3(256), 0, s, g.BH, g.nT,
-                         (const float*)p.tiletot, p.colrec);
-  }
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_base_scan(g, p.tiletot, p.colrec, err, v16, s);
 }
 
 namespace {
@@ -392,15 +459,7 @@ cudaError_t launch_gate_scan(const float* z, int B, int N, int H, int bias_from_
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // The forward's V conversion runs alongside the tile scan; the base scan waits for both.
-  if (v16 && (e = launch_v_to_f16(v16->v, v16->v16, v16->n, err, s)) != cudaSuccess) return e;
-  const int warps_per_block = 8;
-  {
-    TraceScope trace("gate_base_scan", s);
-    e = launch_dependent(gate_base_scan_kernel, dim3((g.BH + warps_per_block - 1) / warps_per_block), dim3(256), 0,
-                         s, g.BH, g.nT, (const float*)tiletot, colrec);
-  }
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_base_scan(g, tiletot, colrec, err, v16, s);
 }
 
 }  // namespace fox

@@ -139,7 +139,9 @@ cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, i
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
                             const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
                             uint32_t* err, cudaStream_t s);
-// V (bf16, n elements) to fp16 into v16, run between the two gate kernels (see launch_v_to_f16).
+// The forward's fp16 copy of V: v (bf16, n elements, a multiple of 8, 16-byte aligned) to v16.
+// Given to the gate launchers, it is done by the base-scan kernel, which runs alongside the
+// tile scan; a magnitude of 65536 or more (outside fp16) sets DEV_ERR_RANGE.
 struct V16Job {
   const void* v;
   void* v16;
@@ -168,11 +170,6 @@ struct AttnFwdArgs {
 inline size_t fwd_v16_offset(const GateLayout& g) { return g.end; }
 inline size_t fwd_v16_bytes(int B, int N, int H, int d) { return (size_t)B * N * H * d * 2; }
 
-// V (bf16, n elements, a multiple of 8, 16-byte aligned) to fp16; a magnitude of 65536 or
-// more (outside fp16) sets DEV_ERR_RANGE in err. Launched as a programmatic dependent of the
-// gate tile scan (which clears err), so that the two run at once; it awaits that kernel's
-// completion before it ends, and the base scan after it waits for it in turn.
-cudaError_t launch_v_to_f16(const void* v, void* v16, size_t n, uint32_t* err, cudaStream_t s);
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs& a, const CUtensorMap* maps /* q, k, v (v16 when set) */, int nT, int Npad,
                                  cudaStream_t s);

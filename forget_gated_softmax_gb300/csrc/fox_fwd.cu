@@ -25,7 +25,8 @@
 //   warps 0-3  softmax + epilogue of Q tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax + epilogue of Q tile 1
 //   warp  8    TMA producer (Q once; K, V and the column-term record per KV tile, 2 stages)
-//   warp  9    TMEM allocator and single-thread MMA issuer
+//   warp  9    TMEM allocator and MMA issuer (the whole warp runs the issue loop, one
+//              elected lane issues)
 //   warps 10-11 V converters: each V tile from bf16 to fp16, in place in shared memory
 //               (only when V is not already in fp16: the caller's workspace normally holds
 //               an fp16 copy, written once by the gate step's base-scan kernel, and these
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
+      const uint32_t leader = elect_lane();  // the one lane that issues (see umma_ss_e)
       constexpr uint32_t tb = L::kTileBytes;
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_f16(128, D, false, true);  // P (TMEM) and V fp16
@@ -363,18 +365,18 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
       }
       auto issue_s = [&](int k, int st) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[k], dA[k][ks], st ? dB[1][ks] : dB[0][ks], idS, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) umma_ss_e(leader, tS[k], dA[k][ks], st ? dB[1][ks] : dB[0][ks], idS, ks > 0);
       };
       auto issue_pv = [&](int k, int st, bool acc) {
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t dv = st ? dVs[1][ks] : dVs[0][ks];
-          umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
+          umma_ts_e(leader, tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
         }
       };
       // One K-step of P V for Q tile k with the V descriptor dv.
       auto pv_ks = [&](int k, int ks, bool acc, uint64_t dv) {
-        umma_ts(tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
+        umma_ts_e(leader, tO[k], tS[k] + ks * 8, dv, idO, (acc || ks > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA) &&
                 mbar_wait(&bars[B_KFULL + 0], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_TMA);
@@ -383,9 +385,9 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
         for (int k = 0; k < 2; ++k)
           if (active[k] && first[k] == 0) {
             issue_s(k, 0);
-            umma_commit(&bars[B_SFULL + k]);
+            umma_commit_e(leader, &bars[B_SFULL + k]);
           }
-        umma_commit(&bars[B_KEMPTY + 0]);
+        umma_commit_e(leader, &bars[B_KEMPTY + 0]);
       }
       for (int s = 0; s < nJ && ok; ++s) {
         const int st = s & 1, nst = (s + 1) & 1;
@@ -413,8 +415,8 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
           if (!ok) return false;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[0], dA[0][ks], dB[NST][ks], idS, ks > 0);
-          umma_commit(&bars[B_SFULL + 0]);
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss_e(leader, tS[0], dA[0][ks], dB[NST][ks], idS, ks > 0);
+          umma_commit_e(leader, &bars[B_SFULL + 0]);
           ok = mbar_wait(&bars[B_PFULL + 1], s & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
           if (!ok) return false;
           tc_fence_after();
@@ -422,11 +424,11 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
           for (int ks = 0; ks < kTile / 16; ++ks) pv_ks(1, ks, s > 0, dVs[ST][ks]);
           // The V stage is free once the last P V reading it retires: released before the next
           // S group so that the following V load (and its conversion) starts earlier.
-          umma_commit(&bars[B_VEMPTY + ST]);
+          umma_commit_e(leader, &bars[B_VEMPTY + ST]);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) umma_ss(tS[1], dA[1][ks], dB[NST][ks], idS, ks > 0);
-          umma_commit(&bars[B_SFULL + 1]);
-          umma_commit(&bars[B_KEMPTY + NST]);
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss_e(leader, tS[1], dA[1][ks], dB[NST][ks], idS, ks > 0);
+          umma_commit_e(leader, &bars[B_SFULL + 1]);
+          umma_commit_e(leader, &bars[B_KEMPTY + NST]);
           return true;
         };
         if (has1 && s >= first0 && s + 1 < end0 && s + 1 < end1) {
@@ -445,22 +447,22 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
             if (s + 1 < end[k]) {
               if (!(ok = wait_next_k())) break;
               issue_s(k, nst);
-              umma_commit(&bars[B_SFULL + k]);
+              umma_commit_e(leader, &bars[B_SFULL + k]);
             } else {
-              umma_commit(&bars[B_OFINAL + k]);
+              umma_commit_e(leader, &bars[B_OFINAL + k]);
             }
           } else if (s + 1 == first[k]) {
             if (!(ok = wait_next_k())) break;
             issue_s(k, nst);
-            umma_commit(&bars[B_SFULL + k]);
+            umma_commit_e(leader, &bars[B_SFULL + k]);
           }
         }
         if (!ok) break;
-        umma_commit(&bars[B_VEMPTY + st]);
-        if (kready) umma_commit(&bars[B_KEMPTY + nst]);
+        umma_commit_e(leader, &bars[B_VEMPTY + st]);
+        if (kready) umma_commit_e(leader, &bars[B_KEMPTY + nst]);
       }
       // Every MMA issued above must retire before tensor memory is freed.
-      umma_commit(&bars[B_DONE]);
+      umma_commit_e(leader, &bars[B_DONE]);
       mbar_wait_drain(&bars[B_DONE], 0);
     }
     __syncwarp();

@@ -46,6 +46,20 @@ bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_f32_3d_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t pitch1,
+                     uint64_t pitch2, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {pitch1, pitch2};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_x_map(CUtensorMap* map, const void* base, int B, int N, int hidden) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -461,8 +475,9 @@ fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, con
   if (st != FOX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  // error word, ticket counter and look-back status records all start at zero
-  if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return FOX_ERR_CUDA;
+  // the error word, and for the look-back kernel its ticket counter and status records, start at zero
+  const bool seq = gate_bwd_streams(p->B, p->N, p->H, p->N, C, R, z, dz);
+  if (cudaMemsetAsync(ws, 0, seq ? kErrWordBytes : need, s) != cudaSuccess) return FOX_ERR_CUDA;
   return launch_gate_bwd(p->B, p->N, p->H, p->N, p->bias_from_j, C, R, z, dz, ws + kErrWordBytes,
                          reinterpret_cast<unsigned*>(ws + kTicketOffset), reinterpret_cast<uint32_t*>(ws), s) ==
                  cudaSuccess

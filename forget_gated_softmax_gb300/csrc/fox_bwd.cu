@@ -1004,6 +1004,149 @@ __global__ void __launch_bounds__(kGateThreads, 3) gate_grad_kernel(int B, int N
   }
 }
 
+// ------------------------------------------------ gate backward, one sequence per CTA
+// The same d a and dz when there are enough (b, head group) sequences to occupy every SM
+// (B ceil(H / 4) >= the SM count): a CTA takes one batch b and kSeqHeads = 4 heads and walks
+// their whole sequence from the last 128-token block to the first, carrying the suffix sum
+// in double-float from block to block, so no CTA waits on another. Warp 0 streams R, C (rows
+// of the 4 heads, [head][token] in shared memory) and z ([token][head]) through kSeqStages
+// stages by TMA; warps 1-4 take 32 tokens each, one token per lane with all 4 heads in
+// registers, so every shared-memory access of theirs is conflict-free. A consumer warp frees
+// the stage as soon as its values are in registers and forms sigmoid(-z) at once, off the
+// scan's path. Per block: x = R - C, the suffix sum within the warp by shuffles and across the
+// four warps through shared memory (fp32, at most 128 terms, as in the look-back kernel),
+// d a = that + the carry (+ C under the j convention), dz = d a sigmoid(-z), stored by each lane
+// as one 16-byte piece of its token's dz row; then the carry takes the block total. Tokens past
+// N arrive as zeros and their dz is not stored. Four heads per CTA (the least whose z row piece,
+// 16 bytes, a tensor copy can move) give the most CTAs, and the number of independent sequences
+// is what sets the rate: each CTA spends about 1 us per block. Large synthetic (B64 H32 N16384,
+// 512 CTAs): 131 us. Measured slower: 8 heads per CTA (171 us; with two 4-head groups of four
+// warps and dz through shared memory, whole 32-byte sectors, 140 us); dz written back by
+// tensor stores (165 us at 8 heads); 6, 8 or 12 stages instead of 4 (135, 140, 236 us);
+// sigmoid(-z) by the fast intrinsics gained 2 %.
+constexpr int kSeqHeads = 4;
+constexpr int kSeqStages = 4;
+constexpr int kSeqConsumers = 4;  // warps of 32 tokens
+constexpr int kSeqThreads = 32 * (1 + kSeqConsumers);
+constexpr int kSeqBoxBytes = kTile * kSeqHeads * 4;                 // one of R, C, z per stage: 2 KB
+constexpr int kSeqStageBytes = 3 * kSeqBoxBytes;  // R, C, z
+constexpr int kSeqSmem = kSeqStages * kSeqStageBytes + 1024 + 512;  // stages, alignment slack, barriers etc.
+
+__global__ void __launch_bounds__(kSeqThreads) gate_grad_seq_kernel(
+    const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_c,
+    const __grid_constant__ CUtensorMap map_z, float* __restrict__ dz, int N, int H, int nT, int bias_from_j,
+    uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSeqStages * kSeqStageBytes);  // FULL[S], FREE[S]
+  float* wt = reinterpret_cast<float*>(bars + 2 * kSeqStages);                      // [2][consumers][heads]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(wt + 2 * kSeqConsumers * kSeqHeads);
+  const int HG = (H + kSeqHeads - 1) / kSeqHeads;
+  const int b = static_cast<int>(blockIdx.x) / HG, h0 = (static_cast<int>(blockIdx.x) % HG) * kSeqHeads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto buf = [&](int s, int which) { return reinterpret_cast<float*>(sm + s * kSeqStageBytes + which * kSeqBoxBytes); };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSeqStages; ++s) {
+      mbar_init(&bars[s], 1);
+      mbar_init(&bars[kSeqStages + s], kSeqConsumers);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dep_wait();  // R and C of the attention kernel
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_r);
+      tma_prefetch_desc(&map_c);
+      tma_prefetch_desc(&map_z);
+      int loaded = 0;
+      for (int i = 0; i < nT; ++i) {  // block k = nT - 1 - i into stage i % S
+        const int s = i % kSeqStages, n = i / kSeqStages;
+        if (n > 0 && !mbar_wait(&bars[kSeqStages + s], (n - 1) & 1, abort_flag, err, DEV_ERR_TIMEOUT_SYNC)) break;
+        const int k = nT - 1 - i;
+        mbar_arrive_expect_tx(&bars[s], 3 * kSeqBoxBytes);
+        tma_load_3d(buf(s, 0), &map_r, &bars[s], k * kTile, h0, b);
+        tma_load_3d(buf(s, 1), &map_c, &bars[s], k * kTile, h0, b);
+        tma_load_3d(buf(s, 2), &map_z, &bars[s], h0, k * kTile, b);
+        loaded = i + 1;
+      }
+      // every load issued must have landed before shared memory is released
+      for (int i = loaded > kSeqStages ? loaded - kSeqStages : 0; i < loaded; ++i)
+        mbar_wait_drain(&bars[i % kSeqStages], (i / kSeqStages) & 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int t = cw * 32 + lane;  // token within the block
+    float chi[kSeqHeads], clo[kSeqHeads];
+#pragma unroll
+    for (int h = 0; h < kSeqHeads; ++h) chi[h] = clo[h] = 0.f;
+    for (int i = 0; i < nT; ++i) {
+      const int s = i % kSeqStages, n = i / kSeqStages;
+      const bool ok = mbar_wait(&bars[s], n & 1, abort_flag, err, DEV_ERR_TIMEOUT_TMA);
+      const float* r = buf(s, 0);
+      const float* c = buf(s, 1);
+      const float* zz = buf(s, 2);
+      float x[kSeqHeads], cv[kSeqHeads], sg[kSeqHeads], zv[kSeqHeads];
+#pragma unroll
+      for (int q = 0; q < kSeqHeads; q += 4) {
+        const float4 z4 = *reinterpret_cast<const float4*>(zz + t * kSeqHeads + q);
+        zv[q] = z4.x, zv[q + 1] = z4.y, zv[q + 2] = z4.z, zv[q + 3] = z4.w;
+      }
+#pragma unroll
+      for (int h = 0; h < kSeqHeads; ++h) {
+        cv[h] = c[h * kTile + t];
+        x[h] = r[h * kTile + t] - cv[h];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kSeqStages + s]);  // R, C and z of the stage are in registers
+#pragma unroll
+      for (int h = 0; h < kSeqHeads; ++h) sg[h] = 1.f / (1.f + expf(zv[h]));  // sigmoid(-z)
+      // inclusive suffix over the warp's tokens t .. 32 cw + 31
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int h = 0; h < kSeqHeads; ++h) {
+          const float y = __shfl_down_sync(0xffffffffu, x[h], o);
+          if (lane + o < 32) x[h] += y;
+        }
+      }
+      float* wb = wt + (i & 1) * kSeqConsumers * kSeqHeads;
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < kSeqHeads; ++h) wb[cw * kSeqHeads + h] = x[h];  // the warp's total
+      }
+      // the warp totals are visible; a failed wait anywhere stops all four warps together
+      if (named_bar_any(1, 32 * kSeqConsumers, !ok)) break;
+      float out[kSeqHeads];
+#pragma unroll
+      for (int h = 0; h < kSeqHeads; ++h) {
+        float later = 0.f, total = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSeqConsumers; ++w) {
+          const float v = wb[w * kSeqHeads + h];
+          total += v;
+          if (w > cw) later += v;
+        }
+        const float da = x[h] + later + (chi[h] + clo[h]);
+        out[h] = (bias_from_j ? da + cv[h] : da) * sg[h];
+        two_sum_acc(chi[h], clo[h], total, 0.f);
+      }
+      const int tg = (nT - 1 - i) * kTile + t;
+      if (tg < N) {
+#pragma unroll
+        for (int q = 0; q < kSeqHeads; q += 4)
+          *reinterpret_cast<float4*>(dz + ((size_t)b * N + tg) * H + h0 + q) =
+              make_float4(out[q], out[q + 1], out[q + 2], out[q + 3]);
+      }
+    }
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLayout& w, const CUtensorMap* maps,
                          cudaStream_t s) {
@@ -1077,11 +1220,40 @@ cudaError_t launch_bwd_d(const AttnBwdArgs& a, const GateLayout& g, const BwdLay
 
 }  // namespace
 
+bool gate_bwd_streams(int B, int N, int H, int stride, const float* colsum, const float* rowsum, const float* z,
+                      const float* dz) {
+  if (B <= 0 || N <= 0 || H <= 0) return false;
+  // tensor-map rules: 16-byte aligned bases and 16-byte multiples for every row pitch
+  auto a16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+  if (!a16(colsum) || !a16(rowsum) || !a16(z) || !a16(dz) || stride % 4 != 0 || H % 4 != 0) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return (long long)B * ((H + kSeqHeads - 1) / kSeqHeads) >= sms;
+}
+
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
                             const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
                             uint32_t* err, cudaStream_t s) {
   const long long BH = (long long)B * H;
   if (BH == 0 || N == 0) return cudaSuccess;
+  if (gate_bwd_streams(B, N, H, stride, colsum, rowsum, z, dz)) {
+    // R, C as [B][H][stride] rows (box 128 tokens x 4 heads); z as [B][N][H] (box 4 heads x 128 tokens)
+    CUtensorMap maps[3];
+    if (!make_f32_3d_map(&maps[0], rowsum, N, H, B, (uint64_t)stride * 4, (uint64_t)stride * H * 4, kTile, kSeqHeads) ||
+        !make_f32_3d_map(&maps[1], colsum, N, H, B, (uint64_t)stride * 4, (uint64_t)stride * H * 4, kTile, kSeqHeads) ||
+        !make_f32_3d_map(&maps[2], z, H, N, B, (uint64_t)H * 4, (uint64_t)N * H * 4, kSeqHeads, kTile))
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gate_grad_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqSmem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = (long long)B * ((H + kSeqHeads - 1) / kSeqHeads);
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int nT = (N + kTile - 1) / kTile;
+    TraceScope trace("bwd_gate", s);
+    e = launch_dependent(gate_grad_seq_kernel, dim3((unsigned)ctas), dim3(kSeqThreads), kSeqSmem, s, maps[0], maps[1],
+                         maps[2], dz, N, H, nT, bias_from_j, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const int nT = (N + kTile - 1) / kTile;
   const long long ctas = (long long)nT * B * ((H + kGateHeads - 1) / kGateHeads);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

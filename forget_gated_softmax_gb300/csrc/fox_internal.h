@@ -136,6 +136,10 @@ cudaError_t launch_gate_cumulative(const void* ws, const GateLayout& g, int B, i
 // d a_t = sum_{s>=t} (R_s - C_s) (+ C_t when bias_from_j), dz = d a_t sigmoid(-z), in one pass with a
 // decoupled look-back; R and C rows of `stride` floats per (b, h). `stat` (B * H * ceil(N / 128)
 // records of kGateStatBytes) and `ticket` must be zero at the launch; err is the error word.
+// True when the gate gradient takes one sequence per CTA (no look-back, no status records or
+// ticket needed): enough (b, 4-head) sequences to occupy every SM, and tensor-map alignment.
+bool gate_bwd_streams(int B, int N, int H, int stride, const float* colsum, const float* rowsum, const float* z,
+                      const float* dz);
 cudaError_t launch_gate_bwd(int B, int N, int H, int stride, int bias_from_j, const float* colsum,
                             const float* rowsum, const float* z, float* dz, void* stat, unsigned* ticket,
                             uint32_t* err, cudaStream_t s);
@@ -239,6 +243,9 @@ size_t window_workspace_bytes(int B, int N, int H);
 // Host helper: 4-D bf16 tensor map over [B, N, H, d] with a box of 64 channels x 1 head x
 // box_rows tokens x 1 batch and 128-byte swizzle. Returns false when the driver entry point is
 // unavailable or encoding fails.
+// fp32 3-D tensor map (d0 innermost; pitches of dims 1 and 2 in bytes), box (box0, box1, 1), no swizzle.
+bool make_f32_3d_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t pitch1,
+                     uint64_t pitch2, uint32_t box0, uint32_t box1);
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows = kTile,
                    bool f16 = false);
 // Host helpers for the gate projection: x [B, N, hidden] with a box of 64 x 128 x 1, and

@@ -150,6 +150,17 @@ def test_train_workload_backward_16_heads():
     check_heads_blocked(wl.TRAIN_BF16, heads, block=512)
 
 
+def test_many_heads_take_one_sequence_per_cta_for_the_gate_gradient():
+    """B ceil(H / 4) >= the SM count: the backward's gate gradient walks each (b, 4-head)
+    sequence in one CTA. N = 260 leaves a ragged last block. Heads from the first, middle and
+    last CTAs, at both ends of a head group, are checked."""
+    w = wl.Workload("many_heads", 80, 260, 12, 64, "bf16", seed=91, gate="head_uniform", lo=-1.0, hi=6.0,
+                    backward=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w.B * ((w.H + 3) // 4) >= sms
+    check_heads_blocked(w, [(0, 0), (0, 7), (0, 8), (0, 11), (39, 3), (40, 9), (79, 4), (79, 11)])
+
+
 @pytest.mark.parametrize("tile_skip", [False, True])
 def test_gate_ready_reuses_the_forward_gate_terms(tile_skip):
     """fox_bwd with gate_ready on the workspace the forward wrote: no gate scan, the same results

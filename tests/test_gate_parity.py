@@ -77,3 +77,29 @@ def test_gate_bwd_from_sums(B, N, H, from_j):
             # fp32 suffix sums over up to N terms of size ~1
             assert np.linalg.norm(g - ref) <= 1e-5 * max(np.linalg.norm(ref), 1e-30), (b, h)
             assert np.all(g[np.isinf(z[b, :, h])] == 0.0)
+
+
+@pytest.mark.parametrize("B,N,H", [(64, 520, 32), (160, 200, 8), (80, 1000, 12), (40, 4096, 32)])
+@pytest.mark.parametrize("from_j", [False, True])
+def test_gate_bwd_one_sequence_per_cta(B, N, H, from_j):
+    """Shapes with at least one (b, 4-head group) sequence per SM take the kernel that walks
+    each sequence in one CTA (no look-back): fewer blocks than pipeline stages (N = 200), three
+    head groups (H = 12), a ragged last block, and 32 blocks. Every head is checked."""
+    import forget_gated_softmax_gb300 as fox
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * ((H + 3) // 4) >= sms and N % 4 == 0 and H % 4 == 0  # the shape qualifies
+    r = np.random.default_rng(2000 + N + from_j)
+    z = _gates(B, N, H, seed=N + 29)
+    R = r.standard_normal((B, H, N)).astype(np.float32)
+    C = r.standard_normal((B, H, N)).astype(np.float32)
+    dz = fox.fox_gate_bwd(torch.from_numpy(z).cuda(), torch.from_numpy(R).cuda(), torch.from_numpy(C).cuda(),
+                          bias_from_j=from_j)
+    torch.cuda.synchronize()
+    got = dz.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for h in range(H):
+            ref = ora.gate_grad_from_sums(R[b, h], C[b, h], z[b, :, h], from_j)
+            g = got[b, :, h]
+            assert np.linalg.norm(g - ref) <= 1e-5 * max(np.linalg.norm(ref), 1e-30), (b, h)
+            assert np.all(g[np.isinf(z[b, :, h])] == 0.0)

@@ -57,6 +57,7 @@ constexpr int kConvWarps = 2;  // V converter warps (one measured 21 % slower on
 __host__ __device__ constexpr int fwd_threads(bool pre_v) { return 320 + (pre_v ? 0 : 32 * kConvWarps); }
 constexpr int kKappaBytes = kColRec * 4;   // 528
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum while the tile max stays within 2^8
+constexpr int kFwdHeadGroup = 16;          // heads whose query blocks are scheduled together
 
 struct FwdKParams {
   int B, N, H, nT, nQB, Npad;
@@ -239,8 +240,22 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  const int qb = p.nQB - 1 - static_cast<int>(blockIdx.x) / BH;  // longest causal rows first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // Work order: groups of kFwdHeadGroup heads, one after the other, and within a group the
+  // longest causal rows first with the group's heads interleaved. The CTAs resident at once
+  // then share few heads, whose K / V streams stay in L2 (long workload 1.477 -> 1.383 ms,
+  // d = 64 mid 67.6 -> 63.4 us against all heads interleaved; groups of 4 or 8 were slower on
+  // the mid workload).
+  int qb, bh;
+  {
+    constexpr int kG = kFwdHeadGroup;
+    const int idx = static_cast<int>(blockIdx.x);
+    const int full = (BH / kG) * kG * p.nQB;
+    const int gsize = idx < full ? kG : BH % kG;
+    const int gbase = idx < full ? (idx / (kG * p.nQB)) * kG : BH - BH % kG;
+    const int r = idx < full ? idx % (kG * p.nQB) : idx - full;
+    qb = p.nQB - 1 - r / gsize;
+    bh = gbase + r % gsize;
+  }
   const int b = bh / p.H, h = bh % p.H;
   // Q tile k covers rows [128*I_k, 128*I_k + 128). KV tiles are streamed in
   // sequence order s = 0, 1, ..., nJ-1 with J = Jtop - s; tile k takes part

@@ -1023,7 +1023,9 @@ __global__ void __launch_bounds__(kGateThreads, 3) gate_grad_kernel(int B, int N
 // 512 CTAs): 131 us. Measured slower: 8 heads per CTA (171 us; with two 4-head groups of four
 // warps and dz through shared memory, whole 32-byte sectors, 140 us); dz written back by
 // tensor stores (165 us at 8 heads); 6, 8 or 12 stages instead of 4 (135, 140, 236 us);
-// sigmoid(-z) by the fast intrinsics gained 2 %.
+// sigmoid(-z) by the fast intrinsics gained 2 %; splitting each sequence between two CTAs (the
+// earlier part first summing the later part's blocks, R and C only) 196 us: a block costs
+// about the same whether it is summed or fully processed.
 constexpr int kSeqHeads = 4;
 constexpr int kSeqStages = 4;
 constexpr int kSeqConsumers = 4;  // warps of 32 tokens

@@ -154,7 +154,8 @@ fox_status fox_fwd_xgate(const fox_params* p, int hidden, const void* q, const v
  * workspace cleared (a stream-ordered cudaMemsetAsync), Delta_i = dO_i . O_i,
  * the fused recompute-and-backward attention kernel (dK, dV, dQ accumulator and
  * the row and column sums of dS), the dQ conversion and the reverse gate scan
- * (one pass, decoupled look-back across 128-token blocks).
+ * (one pass: a decoupled look-back across 128-token blocks or, with at least
+ * one (b, 4-head) sequence per SM, one CTA walking each whole sequence).
  * With non_causal = 1, Delta is not taken from the bf16 O: a pass of its own
  * forms Delta_i = sum_j P_ij dP_ij from S = Q K^T and dP = dO V^T with P
  * recomputed from LSE, in fp32 (the gate gradient is a small difference of
@@ -191,8 +192,8 @@ fox_status fox_gate_scan(const fox_params* p, const float* z, float* c, void* wo
  * (chain rule through D_ij = c_i - c_j of the module's forward; the suffix form
  * holds with or without the causal mask). R, C: [B,H,N] fp32, each (b, h) row
  * contiguous; z, dz: [B,N,H] fp32. The sums are fp32 within 128-token blocks and
- * fp64 across them. Only B, N, H and bias_from_j are read from p. Workspace (block
- * sums): fox_gate_bwd_workspace_bytes(p).
+ * double-float (two fp32 values, about 48 bits) across them. Only B, N, H and
+ * bias_from_j are read from p. Workspace (block sums): fox_gate_bwd_workspace_bytes(p).
  */
 size_t fox_gate_bwd_workspace_bytes(const fox_params* p);
 fox_status fox_gate_bwd(const fox_params* p, const float* z, const float* R, const float* C, float* dz,

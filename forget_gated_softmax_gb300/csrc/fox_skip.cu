@@ -30,56 +30,64 @@ constexpr double kSkipLog2 = 150.0;  // skip below 2^-150 of the row's largest w
 constexpr int kSpanThreads = 512;
 
 // CTA per (tile T, b*H + h): largest row norms of q and k over the tile's
-// rows t < N (fp32 sum of the exact bf16 squares, then sqrtf). Warp per row.
+// rows t < N (fp32 sum of the exact bf16 squares, then sqrtf). Each warp takes 16 rows:
+// all their q and k loads are issued first (rows past N read as zero), each lane forms its
+// partial sums of squares, and one reduce-scatter across the warp (halving rounds) leaves
+// lane l with the full sum of q row l (l < 16) or k row l - 16; the row maxima follow.
 template <int D>
 __global__ void __launch_bounds__(256) tile_norm_kernel(const __nv_bfloat16* __restrict__ q,
                                                         const __nv_bfloat16* __restrict__ k, int N, int H, int nT,
                                                         float* __restrict__ qmax, float* __restrict__ kmax) {
-  constexpr int E = D / 32;  // bf16 per lane
-  constexpr int kRowsPerWarp = kTile / 8;
+  constexpr int E = D / 32;  // bf16 per lane: 4 (D = 128) or 2 (D = 64)
+  constexpr int kRowsPerWarp = kTile / 8;  // 16
   __shared__ float red[2][8];
   const int T = static_cast<int>(blockIdx.x % nT);
   const int bh = static_cast<int>(blockIdx.x / nT);
   const int b = bh / H, h = bh % H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float mq = 0.f, mk = 0.f;
-#pragma unroll 4
+  uint32_t qa[kRowsPerWarp][E / 2], ka[kRowsPerWarp][E / 2];
+#pragma unroll
   for (int rr = 0; rr < kRowsPerWarp; ++rr) {
     const int t = T * kTile + warp * kRowsPerWarp + rr;
-    if (t >= N) break;
     const size_t base = (((size_t)b * N + t) * H + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+      qa[rr][e] = t < N ? reinterpret_cast<const uint32_t*>(q + base)[e] : 0u;
+      ka[rr][e] = t < N ? reinterpret_cast<const uint32_t*>(k + base)[e] : 0u;
+    }
+  }
+  float v[2 * kRowsPerWarp];  // [0, 16): q rows, [16, 32): k rows (this lane's partial sums)
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
     float sq = 0.f, sk = 0.f;
-    if (E == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(q + base);
-      const uint2 c = *reinterpret_cast<const uint2*>(k + base);
-      const uint32_t av[2] = {a.x, a.y}, cv[2] = {c.x, c.y};
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float a0 = __uint_as_float(av[e] << 16), a1 = __uint_as_float(av[e] & 0xffff0000u);
-        const float c0 = __uint_as_float(cv[e] << 16), c1 = __uint_as_float(cv[e] & 0xffff0000u);
-        sq = fmaf(a0, a0, fmaf(a1, a1, sq));
-        sk = fmaf(c0, c0, fmaf(c1, c1, sk));
-      }
-    } else {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(q + base);
-      const uint32_t c = *reinterpret_cast<const uint32_t*>(k + base);
-      const float a0 = __uint_as_float(a << 16), a1 = __uint_as_float(a & 0xffff0000u);
-      const float c0 = __uint_as_float(c << 16), c1 = __uint_as_float(c & 0xffff0000u);
-      sq = fmaf(a0, a0, a1 * a1);
-      sk = fmaf(c0, c0, c1 * c1);
+    for (int e = 0; e < E / 2; ++e) {
+      const float a0 = __uint_as_float(qa[rr][e] << 16), a1 = __uint_as_float(qa[rr][e] & 0xffff0000u);
+      const float c0 = __uint_as_float(ka[rr][e] << 16), c1 = __uint_as_float(ka[rr][e] & 0xffff0000u);
+      sq = fmaf(a0, a0, fmaf(a1, a1, sq));
+      sk = fmaf(c0, c0, fmaf(c1, c1, sk));
     }
+    v[rr] = sq;
+    v[kRowsPerWarp + rr] = sk;
+  }
+  // Reduce-scatter: after the round of width w, lane l holds the partial sums of values
+  // l mod 2w .. for the half it keeps; after five rounds, the full sum of value l.
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
     }
-    mq = fmaxf(mq, sq);
-    mk = fmaxf(mk, sk);
   }
-  if (lane == 0) {
-    red[0][warp] = mq;
-    red[1][warp] = mk;
-  }
+  // lane l now holds the sum of value l: q row l (l < 16) or k row l - 16; maxima per half
+  float m = v[0];
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[0][warp] = m;
+  if (lane == 16) red[1][warp] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     float a = 0.f, c = 0.f;

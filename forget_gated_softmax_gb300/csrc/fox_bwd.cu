@@ -199,7 +199,7 @@ struct BwdLayoutSmem {
   static constexpr int kRsum = kRec + 1024;                    // [3 slots][4 lane quarters][64] row-sum partials
   static constexpr int kCs = kRsum + 3 * 4 * kHalf * 4;        // column-sum exchange, 128 floats
   static constexpr int kBars = kCs + 512;
-  static constexpr int kNumBars = 21;
+  static constexpr int kNumBars = 27;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
@@ -216,8 +216,8 @@ enum BwdBar {
   BB_FINAL = 15,  // every MMA of warp 14 retired (the last dK / dV included)
   BB_BDONE = 16,  // every MMA of warp 13 retired
   BB_KVD = 17,    // +buffer (2): dV, dK of the buffer's half-tile retired (P^T, dS^T read)
-  BB_DSFREE = 19, // +buffer (2): the dS^T smem buffer has been summed, and the dQ block staged
-                  // over it read out by the bulk engine (count 4)
+  BB_DSFREE = 19, // +4 buffer + lane quarter (8): that quarter's rows of the dS^T smem buffer
+                  // have been summed, and the dQ block staged over them read by the bulk engine
 };
 
 __device__ __forceinline__ void sts_f32(uint32_t addr, uint32_t v) {
@@ -308,6 +308,18 @@ __device__ __forceinline__ void pds32(uint32_t tX, int c0, int qoff, int jr, flo
   }
 }
 
+// Work order: groups of kHeadGroup heads, and within a group the key tiles from J = 0
+// (the most query tiles) down, the group's heads interleaved. The CTAs resident at once
+// then share few heads, whose Q / dO streams stay in L2.
+__device__ __forceinline__ void bwd_work_item(int idx, int BH, int nT, int& J, int& bh) {
+  const int full = (BH / kHeadGroup) * kHeadGroup * nT;  // CTAs in complete groups
+  const int gsize = idx < full ? kHeadGroup : BH % kHeadGroup;
+  const int gbase = idx < full ? (idx / (kHeadGroup * nT)) * kHeadGroup : BH - BH % kHeadGroup;
+  const int r = idx < full ? idx % (kHeadGroup * nT) : idx - full;
+  J = r / gsize;
+  bh = gbase + r % gsize;
+}
+
 template <int D, bool kExactSums>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fox_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -323,19 +335,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  // Work order: groups of kHeadGroup heads, and within a group the key tiles from J = 0
-  // (the most query tiles) down, the group's heads interleaved. The CTAs resident at
-  // once then share few heads, whose Q / dO streams stay in L2.
   int J, bh;
-  {
-    const int idx = static_cast<int>(blockIdx.x);
-    const int full = (BH / kHeadGroup) * kHeadGroup * p.nT;  // CTAs in complete groups
-    const int gsize = idx < full ? kHeadGroup : BH % kHeadGroup;
-    const int gbase = idx < full ? (idx / (kHeadGroup * p.nT)) * kHeadGroup : BH - BH % kHeadGroup;
-    const int r = idx < full ? idx % (kHeadGroup * p.nT) : idx - full;
-    J = r / gsize;
-    bh = gbase + r % gsize;
-  }
+  bwd_work_item(static_cast<int>(blockIdx.x), BH, p.nT, J, bh);
   const int b = bh / p.H, h = bh % p.H;
   // Half-tiles of 64 queries: causal, query tiles I = J .. nT-1 (.. imax(J) with tile
   // skipping); non-causal, all of them.
@@ -347,7 +348,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // each iteration instead of holding it in a register (their register budget is full).
   volatile int* G_shared = reinterpret_cast<volatile int*>(sm + L::kMisc + 8);
 
-  if (threadIdx.x == 0) {
+  // The producer thread initialises the barriers and starts the K and V loads (the caller's
+  // inputs) at once, so that they overlap the set-up below.
+  if (warp == 12 && lane == 0) {
     mbar_init(&bars[BB_KV], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[BB_FULL + s], 1);
@@ -359,13 +362,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars[BB_DQ + x], 1);
       mbar_init(&bars[BB_DQFREE + x], 4);
       mbar_init(&bars[BB_KVD + x], 1);
-      mbar_init(&bars[BB_DSFREE + x], 4);
+      for (int w = 0; w < 4; ++w) mbar_init(&bars[BB_DSFREE + x * 4 + w], 1);
     }
     mbar_init(&bars[BB_FINAL], 1);
     mbar_init(&bars[BB_BDONE], 1);
     *abort_flag = 0;
     *G_shared = G;
     fence_mbar_init();
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    tma_prefetch_desc(&tmap_do);
+    mbar_arrive_expect_tx(&bars[BB_KV], 2 * L::kTileBytes + kColRec * 4);
+    for (int x = 0; x < D / 64; ++x) {
+      tma_load_4d(sm + L::kK + x * 16384, &tmap_k, &bars[BB_KV], x * 64, h, J * kTile, b);
+      tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
+    }
   }
   if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
@@ -396,19 +408,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   // This kernel may start while the row kernel before it still runs (launch_dependent): the K and
-  // V tiles are the caller's input and load at once; everything the earlier kernels wrote (the
-  // column record, Delta, rho, the cleared row sums) is read only after grid_dep_wait().
-  if (warp == 12 && lane == 0) {
-    tma_prefetch_desc(&tmap_q);
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
-    tma_prefetch_desc(&tmap_do);
-    mbar_arrive_expect_tx(&bars[BB_KV], 2 * L::kTileBytes + kColRec * 4);
-    for (int x = 0; x < D / 64; ++x) {
-      tma_load_4d(sm + L::kK + x * 16384, &tmap_k, &bars[BB_KV], x * 64, h, J * kTile, b);
-      tma_load_4d(sm + L::kV + x * 16384, &tmap_v, &bars[BB_KV], x * 64, h, J * kTile, b);
-    }
-  }
+  // V tiles are the caller's input and load at once (above); everything the earlier kernels wrote
+  // (the column record, Delta, rho, the cleared row sums) is read only after grid_dep_wait().
   grid_dep_wait();
   grid_dep_trigger();  // the dQ conversion may start launching (it waits for this kernel's results)
 
@@ -549,15 +550,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int x = g & 1;
       const uint32_t tX = tbase + 128 * x + lane_off;
       const int q0 = I_first * kTile + g * kHalf;
-      ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
-      // The first dQ block of g - 1 went over the dS^T buffer of g - 1. Once the bulk engine
-      // has read it (by now it normally has), the elementwise warps may write that buffer for
-      // g + 1. (Waiting for the read right after issuing it stalled them.)
+      // The first dQ block of g - 1 went over this warp's rows of the dS^T buffer of g - 1. Once
+      // the bulk engine has read it (by now it normally has), the elementwise warps of this lane
+      // quarter may write those rows for g + 1. (Waiting for the read right after issuing it
+      // stalled them.)
       if (staged && lane == 0) {
         bulk_wait_read<1>();
-        mbar_arrive(&bars[BB_DSFREE + (x ^ 1)]);
+        mbar_arrive(&bars[BB_DSFREE + (x ^ 1) * 4 + wq]);
       }
       staged = false;
+      ok = mbar_wait(&bars[BB_PDS + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_SYNC);
       // dQ^T first, so that dP^T of g + 2 can follow as early as possible; the row sums below
       // read the dS^T buffer, which the elementwise warps overwrite only after DSFREE.
       ok = ok && mbar_wait(&bars[BB_DQ + x], (g >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
@@ -676,8 +678,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pds32<true, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, rs, rp, rsum, csum, dd);
       else
         pds32<false, kExactSums>(tX, c0, qoff, jr, p.scale2, cj, dlt, rh, rs, rp, rsum, csum, dd);
-      // The readout staged dQ of g - 2 over this dS^T buffer; the bulk engine must have read it.
-      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars[BB_DSFREE + x], ((g - 2) >> 1) & 1, abort_flag,
+      // The readout warp of this lane quarter staged dQ of g - 2 over these rows of the dS^T
+      // buffer; the bulk engine must have read it.
+      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars[BB_DSFREE + x * 4 + wq], ((g - 2) >> 1) & 1, abort_flag,
                                                        p.err, DEV_ERR_TIMEOUT_SYNC)))
         break;
 #pragma unroll
@@ -701,11 +704,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok && ch == 0) p.colsum[(size_t)bh * p.Npad + j] = csum + cs[jr];
     }
     // dK, dV epilogue: scaled, rounded to bf16 and staged in the shared memory of the K and V
-    // tiles (free once every MMA has retired) in the 128-byte-swizzled layout of the output
-    // tensor maps, then written by tensor stores, whole 128-byte row pieces per 64-channel box
-    // (a thread's own 16-byte stores to rows H d apart had cost about 2 us per CTA). The
-    // stores clip rows past N.
-    if (ok) ok = mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+    // tiles in the 128-byte-swizzled layout of the output tensor maps, then written by tensor
+    // stores, whole 128-byte row pieces per 64-channel box (a thread's own 16-byte stores to
+    // rows H d apart had cost about 2 us per CTA). The stores clip rows past N.
+    // dK and dV are complete once the dV / dK MMAs of the last half-tile have retired. The V
+    // tile is free then; the K tile only once that half-tile's dQ^T, which reads K^T, has too.
+    {
+      const int gl = *G_shared - 1;
+      if (ok) ok = mbar_wait(&bars[BB_KVD + (gl & 1)], (gl >> 1) & 1, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA);
+    }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
@@ -714,11 +721,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tdK = tbase + 256 + lane_off, tdV = tbase + 256 + D + lane_off;
       // Two 32-column loads in flight per wait.
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t src = (which == 0 ? tdK : tdV) + e0;
-        const float mul = which == 0 ? p.scale : 1.f;
+      for (int which = 0; which < 2; ++which) {  // dV, then dK
+        if (which == 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars[BB_FINAL], 0, abort_flag, p.err, DEV_ERR_TIMEOUT_MMA));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t src = (which == 1 ? tdK : tdV) + e0;
+        const float mul = which == 1 ? p.scale : 1.f;
         // row jr of the 64-channel box that holds channel e0 (16 KB per box, 128 B per row)
-        const uint32_t row = smem_u32(sm + (which == 0 ? L::kK : L::kV) + (e0 / 64) * 16384) + (uint32_t)jr * 128u;
+        const uint32_t row = smem_u32(sm + (which == 1 ? L::kK : L::kV) + (e0 / 64) * 16384) + (uint32_t)jr * 128u;
 #pragma unroll
         for (int c = 0; c < kCols; c += 64) {
           uint32_t r[2][32];

@@ -57,7 +57,9 @@ constexpr int kConvWarps = 2;  // V converter warps (one measured 21 % slower on
 __host__ __device__ constexpr int fwd_threads(bool pre_v) { return 320 + (pre_v ? 0 : 32 * kConvWarps); }
 constexpr int kKappaBytes = kColRec * 4;   // 528
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a row maximum while the tile max stays within 2^8
-constexpr int kFwdHeadGroup = 16;          // heads whose query blocks are scheduled together
+// Heads whose query blocks are scheduled together: 8 at d = 128, 16 at d = 64.
+template <int D>
+__host__ __device__ constexpr int fwd_head_group() { return D == 128 ? 8 : 16; }
 
 struct FwdKParams {
   int B, N, H, nT, nQB, Npad;
@@ -240,14 +242,15 @@ __global__ void __launch_bounds__(fwd_threads(kPreV), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  // Work order: groups of kFwdHeadGroup heads, one after the other, and within a group the
-  // longest causal rows first with the group's heads interleaved. The CTAs resident at once
-  // then share few heads, whose K / V streams stay in L2 (long workload 1.477 -> 1.383 ms,
-  // d = 64 mid 67.6 -> 63.4 us against all heads interleaved; groups of 4 or 8 were slower on
-  // the mid workload).
+  // Work order: groups of heads, one after the other, and within a group the longest causal
+  // rows first with the group's heads interleaved. The CTAs resident at once then share few
+  // heads, whose K / V streams stay in L2. Against all heads interleaved: long workload
+  // 1.477 -> 1.383 ms with groups of 16; groups of 8 then took its DRAM traffic per launch from
+  // 1.11 to 0.55 GB at the same time, and the d = 128, N = 4096 shapes 1-2 % faster. At d = 64
+  // (mid workload) groups of 16 measured 67.6 -> 63.4 us, groups of 8 slower than all heads.
   int qb, bh;
   {
-    constexpr int kG = kFwdHeadGroup;
+    constexpr int kG = fwd_head_group<D>();
     const int idx = static_cast<int>(blockIdx.x);
     const int full = (BH / kG) * kG * p.nQB;
     const int gsize = idx < full ? kG : BH % kG;

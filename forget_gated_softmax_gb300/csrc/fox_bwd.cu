@@ -1037,7 +1037,9 @@ __global__ void __launch_bounds__(kGateThreads, 3) gate_grad_kernel(int B, int N
 // tensor stores (165 us at 8 heads); 6, 8 or 12 stages instead of 4 (135, 140, 236 us);
 // sigmoid(-z) by the fast intrinsics gained 2 %; splitting each sequence between two CTAs (the
 // earlier part first summing the later part's blocks, R and C only) 196 us: a block costs
-// about the same whether it is summed or fully processed.
+// about the same whether it is summed or fully processed; the consumer warps taking two, three
+// or four blocks per round (one meeting of the four warps per round, 4 to 9 stages) 136-144 us:
+// the rounds of the consumer warps do not set the rate either.
 constexpr int kSeqHeads = 4;
 constexpr int kSeqStages = 4;
 constexpr int kSeqConsumers = 4;  // warps of 32 tokens

@@ -189,11 +189,13 @@ __device__ __forceinline__ float exp_pass_deferred(uint32_t tS, const float* kap
   const float2 nsc = make_float2(-scale2, -scale2), noff = make_float2(-off, -off);
   float2 s = make_float2(0.f, 0.f);  // sums of the even and odd columns
   float mn = INFINITY;                // min_j tn_j = -max_j t_j
+  uint32_t rawb[2][32];               // chunk qt in rawb[qt & 1]; the next chunk loads during this one's arithmetic
+  tmem_ld32(tS, rawb[0]);
 #pragma unroll
   for (int qt = 0; qt < 4; ++qt) {
-    uint32_t raw[32];
-    tmem_ld32(tS + 32 * qt, raw);
     tmem_ld_wait();
+    if (qt + 1 < 4) tmem_ld32(tS + 32 * (qt + 1), rawb[(qt + 1) & 1]);
+    const uint32_t* raw = rawb[qt & 1];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
       const int j = 32 * qt + 4 * j4;

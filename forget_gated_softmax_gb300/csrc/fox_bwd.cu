@@ -578,6 +578,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(&bars[BB_DQFREE + x]);  // the warp's dQ^T is in registers
+      // At d = 64 each readout warp adds its own key quarter's row sums (four times the atomics,
+      // no meeting of the four warps per half-tile: 0.176 -> 0.167 ms at B4 H16 N2048); at
+      // d = 128 one warp adds the four quarters' partials after the meeting (the other way
+      // measured 2 % slower there).
+      constexpr bool kOwnRowSums = D == 64 && !kExactSums;
+      if (kOwnRowSums && !ok) break;
       float r_lo = 0.f, r_hi = 0.f;  // causal: R of queries 2 lane, 2 lane + 1 over this warp's 32 keys
       if (!kExactSums && ok) {
         const uint32_t sdx = smem_u32(sm + L::kDS + x * 16384);
@@ -590,14 +596,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           r_lo = add_bf_lo(r_lo, w);
           r_hi = add_bf_hi(r_hi, w);
         }
-        reinterpret_cast<float2*>(rpart + ((g & 1) * 4 + wq) * kHalf)[lane] = make_float2(r_lo, r_hi);
+        if (kOwnRowSums) {
+          atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane, r_lo);
+          atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane + 1, r_hi);
+          __syncwarp();  // every lane's loads of these rows come before the block staged over them
+        } else {
+          reinterpret_cast<float2*>(rpart + ((g & 1) * 4 + wq) * kHalf)[lane] = make_float2(r_lo, r_hi);
+        }
       }
       // The four readout warps meet once per half-tile (and agree whether to stop).
-      if (named_bar_any(6, 128, !ok)) {
+      if (!kOwnRowSums && named_bar_any(6, 128, !ok)) {
         ok = false;
         break;
       }
-      if (!kExactSums && wq == 0) {  // R of the half-tile's 64 queries: the four key quarters
+      if (!kExactSums && !kOwnRowSums && wq == 0) {  // R of the half-tile's 64 queries: the four key quarters
         const float2* rp2 = reinterpret_cast<const float2*>(rpart + (g & 1) * 4 * kHalf);
         const float2 a = rp2[lane], bq = rp2[kHalf / 2 + lane], c = rp2[kHalf + lane], d2 = rp2[3 * kHalf / 2 + lane];
         atomicAdd(p.rowsum + (size_t)bh * p.Npad + q0 + 2 * lane, (a.x + bq.x) + (c.x + d2.x));

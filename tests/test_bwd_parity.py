@@ -114,10 +114,11 @@ def test_small_shapes(B, N, H, d, from_j):
     check_heads(w)
 
 
-def test_head_groups_with_remainder():
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_groups_with_remainder(d):
     """13 heads: key tiles are scheduled in groups of 8 heads, so this covers one full group
     and a remainder group of 5."""
-    w = wl.Workload("bgroups", 1, 700, 13, 64, "bf16", seed=77, gate="head_linspace", lo=0.0, hi=5.0, sigma=0.5,
+    w = wl.Workload(f"bgroups{d}", 1, 700, 13, d, "bf16", seed=77, gate="head_linspace", lo=0.0, hi=5.0, sigma=0.5,
                     backward=True)
     check_heads(w)
 

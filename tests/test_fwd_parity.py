@@ -103,6 +103,15 @@ def test_small_shapes_bf16(B, N, H, d, from_j):
     check_full(w)
 
 
+@pytest.mark.parametrize("B,N,H,d", [(1, 700, 13, 128), (1, 520, 21, 64)])
+def test_head_groups_with_remainder(B, N, H, d):
+    """Query blocks are scheduled in groups of 8 heads at d = 128 and 16 at d = 64: 13 and 21
+    heads cover one full group and a remainder group of 5, every row checked."""
+    w = wl.Workload(f"fgroups{H}x{d}", B, N, H, d, "bf16", seed=N + H, gate="head_linspace", lo=0.0, hi=5.0,
+                    sigma=0.5)
+    check_full(w)
+
+
 @pytest.mark.parametrize("scale", [0.05, 0.3])
 def test_custom_scale(scale):
     w = wl.Workload("scale", 1, 300, 2, 64, "bf16", seed=11, gate="normal", lo=1.0)
